@@ -1,0 +1,28 @@
+"""Plain CPU oracle of the routed mixture-of-experts layer forward.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the
+benchmark's CPU-baseline leg may import this package.  The library's own
+path never calls it, and the two share no code.  Both sides read the same
+seeded inputs from the `synth` module.
+
+The oracle is slow and obviously correct.  It is plain numpy.  Layer
+arithmetic (dequantisation, SwiGLU, combine) runs in fp64.  Where floating
+point decides an integer, the oracle decides it in fp32, in the order this
+library defines:
+  * the router logits that choose the top-k ids;
+  * the activation codes of the prefill mirror.
+
+Modules:
+  formats  - E2M1 / E4M3 / E8M0 / bf16 decoding, weight dequantisation,
+             activation quantisation (prefill mirror)
+  route    - router logits in the library's fixed fp32 order, softmax, top-k
+  permute  - stable expert-sorted permutation
+  ffn      - grouped SwiGLU expert FFN, weighted combine, whole layer
+  lru      - global LRU slot map over (layer, expert) keys
+
+Parity status: every function is pinned by the `-m "not gpu"` tests in
+tests/test_oracle_*.py against closed forms, library routines, brute force
+or hand-derived golden values, except the softmax weights and the SiLU.
+Those two are pinned only by tolerance against fp64 brute force.
+"""
+from . import formats, route, permute, ffn, lru  # noqa: F401

@@ -1,0 +1,17 @@
+"""Shared test configuration.
+
+Marker `gpu`: the test needs a CUDA device (the parity tests of the CUDA
+path).  Everything else runs on CPU.
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA device")
