@@ -1,0 +1,484 @@
+#!/usr/bin/env python3
+"""Throughput of the routed MoE layer forward on B300, against the roofline and the CPU oracle.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+  * route (logits, top-k, weights);
+  * permute (expert-sorted pairs);
+  * the global-LRU access of the step's experts, on a side stream;
+  * the expert FFN;
+  * the weighted combine to bf16.
+The FFN is timed with the step's experts resident.  In the `stack` workloads
+a step runs the batch through all 8 layers.
+
+Default workload: decode, 128 experts top-8, d 2048, ffn 768, NVFP4, batch 1
+(MoE-layer tokens/s at decode).  Successive steps cycle through 16 distinct
+layer weight sets (5.4 GB).  A layer's weights are re-read only after 15
+other layers' worth of traffic, so its bytes come from HBM, not from the
+126 MB L2.
+
+Output: one JSON line (rank 0).  Under torchrun every rank runs its own
+replica on its own GPU ("scaling": "weak").  The value is the sum over ranks
+of tokens / (max over ranks of the timed region).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOADS = {
+    # name: (Workload, tokens per step, layer copies cycled)
+    "decode": (synth.DECODE, 1, 16),
+    "decode4": (synth.DECODE, 4, 16),
+    "decode16": (synth.DECODE, 16, 16),
+    "prefill": (synth.PREFILL, 8192, 2),
+    "stack1": (synth.STACK, 1, 8),
+    "stack16": (synth.STACK, 16, 8),
+    "stack64": (synth.STACK, 64, 8),
+    "prefill_split": (synth.PREFILL_SPLIT, 16384, 1),
+    "tiny": (synth.TINY, 16, 64),
+}
+METRIC = "MoE-layer tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU baseline sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (weak scaling: independent replicas, no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, ws
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# inputs
+# ---------------------------------------------------------------------------
+class Layer:
+    def __init__(self, wl: synth.Workload, seed: int, device):
+        L = wl.layer
+        self.W = synth.make_experts(L.fmt, L.E, L.d, L.f, seed, device=device)
+        self.wr = synth.make_router(L.E, L.d, seed, device=device)
+        self.bias = torch.from_numpy(synth.make_zipf_bias(L.E, wl.zipf_s, seed)).to(device)
+
+
+def expert_bytes(wl):
+    return synth.expert_bytes(wl.layer.fmt, wl.layer.d, wl.layer.f)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def kernel_hash() -> str:
+    d = os.path.join(ROOT, "sparse_moe_expert_sorted_b300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per FFN call from the committed ncu summary, if it was taken on the current kernels."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get(workload)
+    if not ent or ent.get("kernel_hash") != kernel_hash():
+        return None
+    return ent.get("bytes_per_call")
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def bench_ours(args, rank, ws):
+    import sparse_moe_expert_sorted_b300 as ft
+    ft.lib()  # fails loudly if the library is missing
+    wl, T, n_layers = WORKLOADS[args.workload]
+    L = wl.layer
+    dev = "cuda"
+    dsc = ft.desc(L.E, L.k, L.d, L.f, L.fmt, L.renorm)
+    stack = args.workload.startswith("stack")
+    layers = [Layer(wl, 1000 * (rank + 1) + i, dev) for i in range(n_layers)]
+    n_x = 64
+    xs = [synth.make_x(T, L.d, 77 + 1000 * rank + i, device=dev) for i in range(n_x)]
+    P = T * L.k
+    ids = torch.empty(T, L.k, dtype=torch.int32, device=dev)
+    tw = torch.empty(T, L.k, dtype=torch.float32, device=dev)
+    off = torch.empty(L.E + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(P, dtype=torch.int32, device=dev)
+    pp = torch.empty(P, dtype=torch.int32, device=dev)
+    y = torch.empty(P, L.d, dtype=torch.float32, device=dev)
+    out = torch.empty(T, L.d, dtype=torch.float32, device=dev)
+    out_bf = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
+    ws_r = ft.workspace(ft.route_workspace_size(dsc, T))
+    ws_p = ft.workspace(ft.permute_workspace_size(dsc, T))
+    ws_f = ft.workspace(ft.expert_ffn_workspace_size(dsc, T))
+    ws_l = ft.workspace(ft.layer_workspace_size(dsc, T))
+    structs = [ft.weights_struct(l.W) for l in layers]
+    lru = ft.LRU(wl.layers if stack else 1, L.E, wl.capacity or L.E)
+    cap = min(P, L.E)
+    hit = torch.empty(cap, dtype=torch.uint8, device=dev)
+    lslot = torch.empty(cap, dtype=torch.int32, device=dev)
+    lev = torch.empty(cap, dtype=torch.int32, device=dev)
+    lcnt = torch.zeros(2, dtype=torch.int64, device=dev)
+    main = torch.cuda.Stream()
+    side = torch.cuda.Stream()
+    ev_fork = [torch.cuda.Event() for _ in range(2)]
+
+    def one_layer(li, x, lru_layer):
+        l = layers[li]
+        ft.route(dsc, x, l.wr, l.bias, ids, tw, None, ws_r, main)
+        ft.permute(dsc, ids, off, sp, pp, ws_p, main)
+        # the LRU decision runs beside the FFN on a side stream
+        ev_fork[0].record(main)
+        side.wait_event(ev_fork[0])
+        lru.step(lru_layer, ids, hit, lslot, lev, lcnt, side)
+        ev_fork[1].record(side)
+        ft.expert_ffn(dsc, structs[li], None, x, off, sp, None, y, ws_f, main)
+        ft.combine(dsc, T, y, pp, tw, ids, None, None, out, out_bf, main)
+        main.wait_event(ev_fork[1])
+
+    def step(i):
+        x = xs[i % n_x]
+        if stack:
+            for li in range(n_layers):
+                one_layer(li, x, li)
+        else:
+            one_layer(i % n_layers, x, 0)
+
+    # eager warm-up (also loads every kernel), then capture K steps into one graph
+    with torch.cuda.stream(main):
+        for i in range(max(1, args.warmup)):
+            step(i)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=main):
+        for i in range(K):
+            step(i)
+    for _ in range(max(3, args.warmup // max(1, K) + 1)):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(main)
+    graph.replay()
+    t1.record(main)
+    t1.synchronize()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    ms_max = max_over_ranks(ms, ws)
+    tokens = T * K * ws
+    value = tokens / (ms_max / 1e3)
+    launches_per_layer = 1 + (1 if T > 64 else 0)  # route
+    n_perm = 1 if P <= 1024 else 2
+    launches_per_layer += n_perm + 1 + 2 + 1     # permute, lru, ffn (2), combine
+    gpu_launches = K * launches_per_layer * (n_layers if stack else 1)
+
+    # --- dominant call (expert FFN) timed alone over the same steps ----------
+    n_ffn = min(K, 256)
+    sev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ffn)]
+    eev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ffn)]
+    uniq = []
+    g2 = torch.cuda.CUDAGraph()
+    routes = []
+    with torch.cuda.stream(main):
+        for i in range(n_ffn):
+            li = i % n_layers
+            x = xs[i % n_x]
+            l = layers[li]
+            r_ids = torch.empty_like(ids)
+            r_w = torch.empty_like(tw)
+            r_off = torch.empty_like(off)
+            r_sp = torch.empty_like(sp)
+            r_pp = torch.empty_like(pp)
+            ft.route(dsc, x, l.wr, l.bias, r_ids, r_w, None, ws_r, main)
+            ft.permute(dsc, r_ids, r_off, r_sp, r_pp, ws_p, main)
+            routes.append((li, x, r_ids, r_off, r_sp))
+    torch.cuda.synchronize()
+    for li, x, r_ids, r_off, r_sp in routes:
+        uniq.append(len(np.unique(r_ids.cpu().numpy())))
+    with torch.cuda.graph(g2, stream=main):
+        for i, (li, x, r_ids, r_off, r_sp) in enumerate(routes):
+            sev[i].record(main)
+            ft.expert_ffn(dsc, structs[li], None, x, r_off, r_sp, None, y, ws_f, main)
+            eev[i].record(main)
+    g2.replay()
+    torch.cuda.synchronize()
+    g2.replay()
+    torch.cuda.synchronize()
+    ffn_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(sev, eev)]))
+    eb = expert_bytes(wl)
+    alg_bytes = float(np.mean(uniq)) * eb + T * L.d * 2 + P * L.d * 4
+    peaks, src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    achieved = alg_bytes / (ffn_ms / 1e3) / 1e9
+    path = ft.expert_ffn_path(dsc, T)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4), "traffic": ncu_traffic(args.workload),
+                "kernel": "ftmoe_expert_ffn (gate/up + down kernels)", "peak_source": src,
+                "ffn_us": round(ffn_ms * 1e3, 3), "alg_bytes_per_call": int(alg_bytes),
+                "mean_unique_experts": round(float(np.mean(uniq)), 2)}
+    if path != 0:
+        flops = 2.0 * P * 3 * L.d * L.f
+        ratio = 6.0 if path == 1 else 2.0   # nominal FP4:bf16 and FP8:bf16 dense ratios
+        peak_t = peaks["bf16_tflops"] * ratio
+        ach = flops / (ffn_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": round(peak_t, 1), "unit": "TFLOP/s",
+                    "frac": round(ach / peak_t, 4), "traffic": ncu_traffic(args.workload),
+                    "kernel": "ftmoe_expert_ffn", "peak_source": f"{src} bf16 x {ratio:g} (nominal ratio)",
+                    "ffn_us": round(ffn_ms * 1e3, 3)}
+
+    # --- end to end through the public API with host buffers ------------------
+    e2e = bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, min(K, 200), main)
+
+    res = {
+        "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / K, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {0: "bf16", 1: "nvfp4", 2: "mxfp4", 3: "fp8_e4m3"}[L.fmt] + " weights, fp32 accumulate",
+        "data": "synthetic (seeded; random-init weights)",
+        "config": {"workload": f"{wl.name} T={T}" + (" x8 layers" if stack else ""), "E": L.E, "k": L.k,
+                   "d": L.d, "ffn": L.f, "tokens_per_step": T, "layers_cycled": n_layers,
+                   "l2": f"weights > L2: {n_layers} distinct layer copies cycled "
+                         f"({n_layers * L.E * eb / 1e9:.1f} GB)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clk,
+    }
+    lru.close()
+    return res
+
+
+def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
+    """Same metric through ftmoe_layer_forward with pinned host inputs and outputs."""
+    dev = "cuda"
+    xh = [synth.make_x(T, L.d, 555 + i).pin_memory() for i in range(8)]
+    oh = torch.empty(T, L.d, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
+    of = torch.empty(T, L.d, dtype=torch.float32, device=dev)
+    ob = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
+    ids = torch.empty(T, L.k, dtype=torch.int32, device=dev)
+    tw = torch.empty(T, L.k, dtype=torch.float32, device=dev)
+    ws = ft.workspace(ft.layer_workspace_size(dsc, T))
+
+    def step(i):
+        with torch.cuda.stream(main):
+            xd.copy_(xh[i % len(xh)], non_blocking=True)
+            lis = range(n_layers) if stack else [i % n_layers]
+            for li in lis:
+                l = layers[li]
+                ft.layer_forward(dsc, structs[li], None, xd, l.wr, l.bias, ids, tw, of, ob, ws, main)
+            oh.copy_(ob, non_blocking=True)
+
+    for i in range(5):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(i)
+    main.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": round(T * steps / dt, 3), "unit": "tokens/s", "h2d_bytes_per_step": T * L.d * 2,
+            "d2h_bytes_per_step": T * L.d * 2, "steps": steps,
+            "how": "per step: pinned H2D of x, ftmoe_layer_forward per layer, D2H of the bf16 output; wall clock"}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_rate(workload: str, budget_s: float, max_steps: int | None = None):
+    """Oracle tokens/s on a bounded sample of the workload (host cores)."""
+    from oracle import ffn as OF
+    from threadpoolctl import threadpool_info
+    wl, T, n_layers = WORKLOADS[workload]
+    L = wl.layer
+    stack = workload.startswith("stack")
+    # one layer's weights on the host; the oracle dequantises each expert inside the timed region
+    Wt = synth.make_experts(L.fmt, L.E, L.d, L.f, 4242, device="cuda" if torch.cuda.is_available() else "cpu")
+    W = dict(fmt=L.fmt, d=L.d, f=L.f, glob=Wt.glob.cpu().numpy())
+    for name in ("gate", "up", "down"):
+        t = getattr(Wt, name).cpu()
+        W[name] = t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+        s = getattr(Wt, name + "_s")
+        W[name + "_s"] = None if s is None else s.cpu().numpy()
+    del Wt
+    wr = synth.make_router(L.E, L.d, 4242).view(torch.int16).numpy().view(np.uint16)
+    bias = synth.make_zipf_bias(L.E, wl.zipf_s, 4242)
+    slot = np.arange(L.E)
+    sample_T = T if T <= 64 else 256                       # prefill: a 256-token sample of the chunk
+    done_tokens = 0
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        x = synth.make_x(sample_T, L.d, 900 + steps).view(torch.int16).numpy().view(np.uint16)
+        for _ in range(n_layers if stack else 1):
+            OF.layer(W, slot, x, wr, bias, L.k, L.renorm)
+        done_tokens += sample_T
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_steps and steps >= max_steps):
+            break
+    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    sample = (f"{steps} oracle step(s) of {sample_T} token(s)" + (" x 8 layers" if stack else "") +
+              f" ({'the full batch' if sample_T == T else f'a {sample_T}-token sample of the {T}-token chunk'})")
+    return done_tokens / el, threads, sample, el
+
+
+def bench_reference(args, rank, ws):
+    wl, T, n_layers = WORKLOADS[args.workload]
+    budget = min(150.0, max(10.0, 0.05 * args.steps))
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle_rate(args.workload, 0.0, max_steps=1)
+    rate, threads, sample, el = oracle_rate(args.workload, budget, max_steps=args.steps)
+    value = rate
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * T / rate, 3) if rate else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; random-init weights)",
+            "config": {"workload": f"{wl.name} T={T}" + (" x8 layers" if args.workload.startswith("stack") else ""),
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        # the oracle runs on the host cores of rank 0 only; other ranks exit without work
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(bench_reference(args, 0, 1)), flush=True)
+        return
+    rank, ws = dist_init()
+    res = bench_ours(args, rank, ws)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            rate, threads, sample, _ = oracle_rate(args.workload, args.cpu_seconds)
+            res["cpu_baseline"] = {"value": round(rate, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                   "sample": sample}
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,262 @@
+/*
+ * ftmoe.h - C ABI of the routed mixture-of-experts layer forward on B300 (sm_103a).
+ *
+ * The layer follows the FreeToken pages' statement of the problem:
+ *   - a small router picks a handful of experts per token, e.g. 6 of 256
+ *     (banandre.com, "The 284B Model on a 32GB GPU Trick", section
+ *     "Sparsity Is a Lie (But a Useful One)");
+ *   - resident experts run on GPU tensor cores from expert slots, with weights
+ *     in MXFP4, NVFP4, FP8 or BF16 (zubnet.ai, "FreeToken, Unsloth GGUF ...
+ *     consumer hardware");
+ *   - partial sums over a split of the selected experts merge exactly once the
+ *     layer completes (banandre.com, same page, section "The q* Policy: Math
+ *     Instead of Guesses");
+ *   - a global LRU over all MoE layers, updated on every miss, decides which
+ *     experts are resident (asapai.co.kr, "Running 753B GLM-5.2 on a single
+ *     workstation GPU", section "Abandoning fixed offloading in favor of
+ *     measured bandwidth"; banandre.com, section "Semantic-Aware Caching").
+ *
+ * Conventions for every call
+ *   - Pointers are DEVICE pointers unless a parameter says "host".  The caller
+ *     owns all memory.  The library never allocates or frees caller memory.
+ *   - Scratch is passed as (ws, ws_bytes).  Its size comes from the matching
+ *     *_workspace_size query.  Before its first use, the workspace's first
+ *     FTMOE_WS_ZERO_BYTES bytes must be zero.  Every call leaves them zero
+ *     again (they hold completion counters).  One workspace must not be used by
+ *     two calls that can run at the same time.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on it.  Kernels are launched with programmatic dependent
+ *     launch, so consecutive calls on one stream overlap their launch latency.
+ *   - Layouts are row-major and contiguous.  bf16 values travel as uint16_t
+ *     bit patterns.
+ *   - Argument errors are found on the host before any launch, and return
+ *     FTMOE_ERR_INVALID_ARG without touching memory.  Data errors found on the
+ *     device (an id or slot out of range) never trap.  They set a device error
+ *     word, which ftmoe_get_device_error reads and clears; the offending item
+ *     is skipped.
+ */
+#ifndef FTMOE_H
+#define FTMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FTMOE_WS_ZERO_BYTES 256
+
+typedef enum {
+  FTMOE_OK = 0,
+  FTMOE_ERR_INVALID_ARG = 1,   /* bad pointer, size or descriptor (host check) */
+  FTMOE_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement */
+  FTMOE_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+  FTMOE_ERR_WORKSPACE = 4,     /* ws_bytes below the *_workspace_size answer */
+  FTMOE_ERR_TIMEOUT = 5,       /* a bounded device wait gave up */
+  FTMOE_ERR_DEVICE_CHECK = 6   /* a device-side data check failed */
+} ftmoe_status;
+
+/* Expert weight storage formats.  K is the reduction dim, innermost in memory.
+ *   BF16      w = bf16 value
+ *   NVFP4     E2M1 codes, 2 per byte (element 2i = low nibble), one E4M3 scale
+ *             per 16 consecutive K elements [N][K/16], one fp32 scale per tensor:
+ *             w = e2m1 * e4m3 * tensor_scale
+ *   MXFP4     E2M1 codes as above, one E8M0 scale per 32 K elements [N][K/32]:
+ *             w = e2m1 * 2^(e8m0 - 127)
+ *   FP8_B128  E4M3 codes [N][K], one fp32 scale per 128x128 block [N/128][K/128]:
+ *             w = e4m3 * scale
+ */
+typedef enum { FTMOE_BF16 = 0, FTMOE_NVFP4 = 1, FTMOE_MXFP4 = 2, FTMOE_FP8_B128 = 3 } ftmoe_wfmt;
+
+/* One MoE layer: E routed experts, top-k, model width d, expert width ffn. */
+typedef struct {
+  int E;        /* 1..1024 */
+  int k;        /* 1..min(E, 32) */
+  int d;        /* multiple of 256 */
+  int ffn;      /* multiple of 128 */
+  int fmt;      /* ftmoe_wfmt of the expert weights */
+  int renorm;   /* 1: the k weights are divided by their sum; 0: raw softmax probabilities */
+} ftmoe_layer_desc;
+
+/* Expert weights of C slots (the slot arena).  Slot s of each array starts
+ * at s times the per-slot size of that array:
+ *   gate, up      [C][ffn][d]  codes (bf16: uint16; FP4: d/2 bytes per row; FP8: d bytes)
+ *   down          [C][d][ffn]  codes
+ *   *_scale       NVFP4: uint8 E4M3 [C][N][K/16]; MXFP4: uint8 E8M0 [C][N][K/32];
+ *                 FP8_B128: float [C][N/128][K/128]; BF16: NULL
+ *   tensor_scale  NVFP4: float [C][3] (gate, up, down); otherwise NULL
+ * Every pointer must be 16-byte aligned. */
+typedef struct {
+  int fmt;
+  int C;
+  int d;
+  int ffn;
+  const void* gate;
+  const void* up;
+  const void* down;
+  const void* gate_scale;
+  const void* up_scale;
+  const void* down_scale;
+  const float* tensor_scale;
+} ftmoe_weights;
+
+/* ---------------------------------------------------------------------------
+ * a1  ftmoe_route - router logits, top-k ids and their weights.
+ * Pages: a tiny router selects a handful of experts for each token
+ * (banandre.com, "The 284B Model on a 32GB GPU Trick", section "Sparsity Is a
+ * Lie (But a Useful One)").  Reading: softmax over all E logits, then top-k;
+ * ties go to the lower id.
+ *   x          bf16 [T][d]
+ *   w_router   bf16 [E][d]
+ *   logit_bias fp32 [E] or NULL (added after the dot product)
+ *   topk_ids   int32 [T][k]: ordered by (logit desc, id asc)
+ *   topk_w     fp32 [T][k]: softmax probability of each chosen expert,
+ *              divided by their sum when desc->renorm
+ *   logits     fp32 [T][E] or NULL
+ * The fp32 logit has one fixed definition (order R), so the ids are
+ * reproducible bit for bit:
+ *   - Chunk c = elements 8c..8c+7 belongs to lane c % 32.
+ *   - Each lane sums its products in ascending element order from 0.0f.
+ *     Each product is exact; each add is rounded to fp32.
+ *   - The 32 lane sums combine by an xor butterfly over offsets 16, 8, 4, 2, 1.
+ *   - The bias is added last.
+ * Preconditions: 1 <= T <= 2^20, d % 256 == 0.
+ * ------------------------------------------------------------------------- */
+size_t ftmoe_route_workspace_size(const ftmoe_layer_desc* desc, int T);
+ftmoe_status ftmoe_route(const ftmoe_layer_desc* desc, const uint16_t* x, const uint16_t* w_router,
+                         const float* logit_bias, int T, int32_t* topk_ids, float* topk_w, float* logits,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * a2  ftmoe_permute - stable expert-sorted permutation of the P = T*k pairs.
+ * The pages do not describe it.  It is what computing each selected expert
+ * once over a batch needs (banandre.com, section "Sparsity Is a Lie").
+ *   topk_ids        int32 [T][k], every id in [0, E)
+ *   expert_offsets  int32 [E+1]: exclusive prefix sum of per-expert counts
+ *   sorted_pair     int32 [P]: pair indices p = t*k + r ordered by (expert, p)
+ *   pair_pos        int32 [P]: position of pair p in sorted_pair
+ * An id outside [0, E) sets FTMOE_ERR_DEVICE_CHECK and is counted as expert E-1.
+ * ------------------------------------------------------------------------- */
+size_t ftmoe_permute_workspace_size(const ftmoe_layer_desc* desc, int T);
+ftmoe_status ftmoe_permute(const ftmoe_layer_desc* desc, const int32_t* topk_ids, int T,
+                           int32_t* expert_offsets, int32_t* sorted_pair, int32_t* pair_pos,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * a3+a4  ftmoe_expert_ffn - grouped SwiGLU FFN of the resident experts.
+ * Pages: resident experts are computed on GPU tensor cores from expert slots
+ * (zubnet.ai, "FreeToken, Unsloth GGUF ... consumer hardware").
+ * For each expert e with slot_of[e] >= 0, over its rows
+ * sorted_pair[expert_offsets[e] .. expert_offsets[e+1]):
+ *   h = silu(X W_gate^T) * (X W_up^T),   y = h W_down^T
+ * where X holds the rows x[p / k] of those pairs.  Experts with slot_of[e] < 0
+ * are skipped: that is one side of an exact split.
+ *   slot_of   int32 [E]: slot index in `weights`, or -1
+ *   topk_w    NULL: y_or_out is y, fp32 [P][d] in sorted order (row j = pair
+ *             sorted_pair[j]); rows of skipped experts are left untouched
+ *             otherwise: fused combine.  y_or_out is out fp32 [T][d], and
+ *             w[p] * y is ADDED into it (zero it first, or pass a partial to merge)
+ * T at or above the prefill threshold runs the tensor-core path: activations
+ * and h are quantised to NVFP4 (NVFP4 weights) or FP8 (FP8_B128 weights) by
+ * the library's stated rule.  Smaller T runs the weight-only streaming path.
+ * ------------------------------------------------------------------------- */
+size_t ftmoe_expert_ffn_workspace_size(const ftmoe_layer_desc* desc, int T);
+/* Which path ftmoe_expert_ffn takes for this layer and T: 0 = weight-only streaming
+ * on CUDA cores (no activation quantisation), 1 = tensor cores with NVFP4
+ * activations, 2 = tensor cores with FP8 activations.  -1 = invalid descriptor. */
+int ftmoe_expert_ffn_path(const ftmoe_layer_desc* desc, int T);
+ftmoe_status ftmoe_expert_ffn(const ftmoe_layer_desc* desc, const ftmoe_weights* weights,
+                              const int32_t* slot_of, const uint16_t* x, int T,
+                              const int32_t* expert_offsets, const int32_t* sorted_pair,
+                              const float* topk_w, float* y_or_out,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * a5  ftmoe_combine - weighted combine and exact merge.
+ * Pages: the partial sums over a split of the selected experts merge exactly
+ * once the layer completes (banandre.com, section "The q* Policy").
+ *   out_t = partial_b_t + sum_{r: slot_of[ids[t,r]] >= 0} w[t,r] * y[pair_pos[t*k+r]]
+ * summed in ascending r, in fp32.
+ *   y          fp32 [P][d] sorted rows, or NULL (then out = partial_b, a cast/merge only)
+ *   slot_of    int32 [E] or NULL (= every expert resident)
+ *   partial_b  fp32 [T][d] or NULL
+ *   out_f32    fp32 [T][d] or NULL; out_bf16 bf16 [T][d] or NULL (round to nearest even)
+ * ------------------------------------------------------------------------- */
+ftmoe_status ftmoe_combine(const ftmoe_layer_desc* desc, int T, const float* y, const int32_t* pair_pos,
+                           const float* topk_w, const int32_t* topk_ids, const int32_t* slot_of,
+                           const float* partial_b, float* out_f32, uint16_t* out_bf16, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * a6  global LRU slot map over (layer, expert) keys, key = layer*E + e.
+ * Pages: in decode the expert cache is a global LRU updated on every miss
+ * (asapai.co.kr, "Running 753B GLM-5.2 on a single workstation GPU", section
+ * "Abandoning fixed offloading in favor of measured bandwidth").  It spans all
+ * MoE layers (banandre.com, section "Semantic-Aware Caching").  It starts
+ * cold (banandre.com, section "Elastic Memory").
+ * Reading:
+ *   - Each call makes one access per unique expert of topk_ids, in ascending id order.
+ *   - A hit refreshes the key's recency.
+ *   - A miss takes the lowest free slot, else evicts the least recently used key
+ *     and takes its slot.
+ * The handle owns its device state: slot_of [L][E], key per slot, recency list.
+ * ------------------------------------------------------------------------- */
+typedef struct ftmoe_lru ftmoe_lru;
+
+/* L layers, E experts per layer, C slots.  The state is processed in shared memory,
+ * so (L*E + 3*C) * 4 bytes must stay within 200 KiB (else FTMOE_ERR_UNSUPPORTED).
+ * Allocates the handle's device state. */
+ftmoe_status ftmoe_lru_create(int L, int E, int C, ftmoe_lru** out);
+/* Empties the table (cold start).  Asynchronous on stream. */
+ftmoe_status ftmoe_lru_reset(ftmoe_lru* lru, void* stream);
+/* Synchronises the device, then frees the state. */
+ftmoe_status ftmoe_lru_destroy(ftmoe_lru* lru);
+/* Device pointer to the handle's slot_of table, int32 [L][E] (-1 = not resident).
+ * Row l is the slot_of argument of ftmoe_expert_ffn for layer l. */
+const int32_t* ftmoe_lru_slot_of(const ftmoe_lru* lru);
+/* Copies the slot_of table into dst (device, int32 [L][E]); asynchronous on stream. */
+ftmoe_status ftmoe_lru_copy_slot_of(const ftmoe_lru* lru, int32_t* dst, void* stream);
+
+/* One call: the accesses of (layer, topk_ids [B][k]).  Outputs are per access,
+ * in access order.  Size them for min(B*k, E) entries:
+ *   hit uint8, slot int32, evicted_key int32 (-1 = none)
+ *   counters int64 [2]: the handle's running totals (accesses, misses) after the call */
+ftmoe_status ftmoe_slot_lru(ftmoe_lru* lru, int layer, const int32_t* topk_ids, int B, int k,
+                            uint8_t* hit, int32_t* slot, int32_t* evicted_key, int64_t* counters,
+                            void* stream);
+/* A whole trace int32 [steps][L][B][k] in one launch, steps outer, layers inner.
+ * Outputs hold every access of the trace in order; capacity (host) is their length.
+ *   counters int64 [2]: running totals (accesses, misses); at most `capacity`
+ *   accesses are written.  Needing more sets FTMOE_ERR_DEVICE_CHECK. */
+ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* lru, const int32_t* trace, int steps, int B, int k,
+                                   uint8_t* hit, int32_t* slot, int32_t* evicted_key, int64_t capacity,
+                                   int64_t* counters, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Whole layer in one call: route -> permute -> expert FFN (fused combine) -> bf16.
+ * This is the same work as the four calls above, on one workspace.
+ *   slot_of    int32 [E] or NULL (every expert resident in slot e)
+ *   topk_ids, topk_w  outputs as in ftmoe_route (may be NULL only together)
+ *   out_f32    fp32 [T][d] (required: the accumulator);  out_bf16  bf16 [T][d] or NULL
+ * ------------------------------------------------------------------------- */
+size_t ftmoe_layer_workspace_size(const ftmoe_layer_desc* desc, int T);
+ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* desc, const ftmoe_weights* weights,
+                                 const int32_t* slot_of, const uint16_t* x, const uint16_t* w_router,
+                                 const float* logit_bias, int T, int32_t* topk_ids, float* topk_w,
+                                 float* out_f32, uint16_t* out_bf16, void* ws, size_t ws_bytes,
+                                 void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Helpers
+ * ------------------------------------------------------------------------- */
+const char* ftmoe_status_string(ftmoe_status s);
+/* Reads and clears the device error word (synchronises `stream`).
+ * *code = 0 if no device-side check failed since the last read. */
+ftmoe_status ftmoe_get_device_error(int* code, void* stream);
+/* Library version, e.g. 100 = 0.1.0. */
+int ftmoe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FTMOE_H */

@@ -1,0 +1,253 @@
+"""Python binding of the ftmoe C ABI (include/ftmoe.h).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels
+of libftmoe.so.  Tensors are torch CUDA tensors (device memory); streams are
+torch CUDA streams.  Nothing here computes the layer: there is no CPU or
+PyTorch fallback.  If the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+__all__ = [
+    "BF16", "NVFP4", "MXFP4", "FP8_B128", "LayerDesc", "FtmoeError", "lib", "route", "permute", "expert_ffn",
+    "combine", "layer_forward", "LRU", "weights_struct", "workspace", "get_device_error",
+]
+
+BF16, NVFP4, MXFP4, FP8_B128 = 0, 1, 2, 3
+WS_ZERO_BYTES = 256
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libftmoe.so")
+
+# Symbols declared in include/ftmoe.h (checked by the ABI test).
+EXPORTS = [
+    "ftmoe_route_workspace_size", "ftmoe_route", "ftmoe_permute_workspace_size", "ftmoe_permute",
+    "ftmoe_expert_ffn_workspace_size", "ftmoe_expert_ffn_path", "ftmoe_expert_ffn", "ftmoe_combine", "ftmoe_lru_create", "ftmoe_lru_reset",
+    "ftmoe_lru_destroy", "ftmoe_lru_slot_of", "ftmoe_lru_copy_slot_of", "ftmoe_slot_lru", "ftmoe_slot_lru_replay",
+    "ftmoe_layer_workspace_size", "ftmoe_layer_forward", "ftmoe_status_string", "ftmoe_get_device_error",
+    "ftmoe_version",
+]
+
+
+class FtmoeError(RuntimeError):
+    pass
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("E", ctypes.c_int), ("k", ctypes.c_int), ("d", ctypes.c_int), ("ffn", ctypes.c_int),
+                ("fmt", ctypes.c_int), ("renorm", ctypes.c_int)]
+
+
+class WeightsStruct(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int), ("C", ctypes.c_int), ("d", ctypes.c_int), ("ffn", ctypes.c_int),
+                ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p),
+                ("gate_scale", ctypes.c_void_p), ("up_scale", ctypes.c_void_p), ("down_scale", ctypes.c_void_p),
+                ("tensor_scale", ctypes.c_void_p)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libftmoe.so (raises FtmoeError if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise FtmoeError(f"libftmoe.so is missing ({LIB_PATH}); run `python -m sparse_moe_expert_sorted_b300.build`")
+    L = ctypes.CDLL(LIB_PATH)
+    sig = {
+        "ftmoe_route_workspace_size": (_SZ, [_P, _I]),
+        "ftmoe_route": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
+        "ftmoe_permute_workspace_size": (_SZ, [_P, _I]),
+        "ftmoe_permute": (_I, [_P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
+        "ftmoe_expert_ffn_workspace_size": (_SZ, [_P, _I]),
+        "ftmoe_expert_ffn_path": (_I, [_P, _I]),
+        "ftmoe_expert_ffn": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+        "ftmoe_combine": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+        "ftmoe_lru_create": (_I, [_I, _I, _I, ctypes.POINTER(_P)]),
+        "ftmoe_lru_reset": (_I, [_P, _P]),
+        "ftmoe_lru_destroy": (_I, [_P]),
+        "ftmoe_lru_slot_of": (_P, [_P]),
+        "ftmoe_lru_copy_slot_of": (_I, [_P, _P, _P]),
+        "ftmoe_slot_lru": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P, _P]),
+        "ftmoe_slot_lru_replay": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, ctypes.c_int64, _P, _P]),
+        "ftmoe_layer_workspace_size": (_SZ, [_P, _I]),
+        "ftmoe_layer_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+        "ftmoe_status_string": (ctypes.c_char_p, [_I]),
+        "ftmoe_get_device_error": (_I, [ctypes.POINTER(_I), _P]),
+        "ftmoe_version": (_I, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = lib().ftmoe_status_string(status).decode()
+        raise FtmoeError(f"{what}: {msg} (status {status})")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise FtmoeError("ftmoe takes CUDA tensors (device memory)")
+    if not t.is_contiguous():
+        raise FtmoeError("ftmoe takes contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def desc(E, k, d, ffn, fmt, renorm=1) -> LayerDesc:
+    return LayerDesc(E, k, d, ffn, fmt, renorm)
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A workspace buffer: zero-filled, so its counter header starts at zero."""
+    return torch.zeros(max(int(nbytes), WS_ZERO_BYTES), dtype=torch.uint8, device=device)
+
+
+@dataclass
+class Weights:
+    """Expert slot arena tensors (any object with these attributes works)."""
+    fmt: int
+    d: int
+    f: int
+    gate: torch.Tensor
+    up: torch.Tensor
+    down: torch.Tensor
+    gate_s: torch.Tensor | None
+    up_s: torch.Tensor | None
+    down_s: torch.Tensor | None
+    glob: torch.Tensor
+
+
+def weights_struct(W) -> WeightsStruct:
+    """ftmoe_weights view of an arena with attributes fmt, d, f, gate, up, down,
+    gate_s, up_s, down_s, glob (tensor scale [C, 3], NVFP4 only)."""
+    return WeightsStruct(W.fmt, W.gate.shape[0], W.d, W.f, _ptr(W.gate), _ptr(W.up), _ptr(W.down),
+                         _ptr(W.gate_s), _ptr(W.up_s), _ptr(W.down_s), _ptr(W.glob) if W.fmt == NVFP4 else None)
+
+
+def route_workspace_size(dsc: LayerDesc, T: int) -> int:
+    return lib().ftmoe_route_workspace_size(ctypes.byref(dsc), T)
+
+
+def route(dsc, x, w_router, bias, ids, w, logits, ws, stream=None):
+    T = x.shape[0]
+    _check(lib().ftmoe_route(ctypes.byref(dsc), _ptr(x), _ptr(w_router), _ptr(bias), T, _ptr(ids), _ptr(w),
+                             _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)), "ftmoe_route")
+
+
+def permute_workspace_size(dsc: LayerDesc, T: int) -> int:
+    return lib().ftmoe_permute_workspace_size(ctypes.byref(dsc), T)
+
+
+def permute(dsc, ids, offsets, sorted_pair, pair_pos, ws, stream=None):
+    T = ids.shape[0]
+    _check(lib().ftmoe_permute(ctypes.byref(dsc), _ptr(ids), T, _ptr(offsets), _ptr(sorted_pair), _ptr(pair_pos),
+                               _ptr(ws), ws.numel(), _stream(stream)), "ftmoe_permute")
+
+
+def expert_ffn_workspace_size(dsc: LayerDesc, T: int) -> int:
+    return lib().ftmoe_expert_ffn_workspace_size(ctypes.byref(dsc), T)
+
+
+def expert_ffn_path(dsc: LayerDesc, T: int) -> int:
+    """0 = weight-only streaming path, 1 = tensor cores with NVFP4 activations, 2 = with FP8 activations."""
+    return lib().ftmoe_expert_ffn_path(ctypes.byref(dsc), T)
+
+
+def expert_ffn(dsc, wstruct, slot_of, x, offsets, sorted_pair, topk_w, y_or_out, ws, stream=None):
+    T = x.shape[0]
+    _check(lib().ftmoe_expert_ffn(ctypes.byref(dsc), ctypes.byref(wstruct), _ptr(slot_of), _ptr(x), T,
+                                  _ptr(offsets), _ptr(sorted_pair), _ptr(topk_w), _ptr(y_or_out), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "ftmoe_expert_ffn")
+
+
+def combine(dsc, T, y, pair_pos, topk_w, topk_ids, slot_of, partial_b, out_f32, out_bf16, stream=None):
+    _check(lib().ftmoe_combine(ctypes.byref(dsc), T, _ptr(y), _ptr(pair_pos), _ptr(topk_w), _ptr(topk_ids),
+                               _ptr(slot_of), _ptr(partial_b), _ptr(out_f32), _ptr(out_bf16), _stream(stream)),
+           "ftmoe_combine")
+
+
+def layer_workspace_size(dsc: LayerDesc, T: int) -> int:
+    return lib().ftmoe_layer_workspace_size(ctypes.byref(dsc), T)
+
+
+def layer_forward(dsc, wstruct, slot_of, x, w_router, bias, ids, topk_w, out_f32, out_bf16, ws, stream=None):
+    T = x.shape[0]
+    _check(lib().ftmoe_layer_forward(ctypes.byref(dsc), ctypes.byref(wstruct), _ptr(slot_of), _ptr(x),
+                                     _ptr(w_router), _ptr(bias), T, _ptr(ids), _ptr(topk_w), _ptr(out_f32),
+                                     _ptr(out_bf16), _ptr(ws), ws.numel(), _stream(stream)), "ftmoe_layer_forward")
+
+
+def get_device_error(stream=None) -> int:
+    code = ctypes.c_int(0)
+    _check(lib().ftmoe_get_device_error(ctypes.byref(code), _stream(stream)), "ftmoe_get_device_error")
+    return code.value
+
+
+class LRU:
+    """Global LRU slot map handle (device state owned by the library)."""
+
+    def __init__(self, L: int, E: int, C: int):
+        self.L, self.E, self.C = L, E, C
+        h = ctypes.c_void_p()
+        _check(lib().ftmoe_lru_create(L, E, C, ctypes.byref(h)), "ftmoe_lru_create")
+        self._h = h
+
+    def reset(self, stream=None):
+        _check(lib().ftmoe_lru_reset(self._h, _stream(stream)), "ftmoe_lru_reset")
+
+    def slot_of_ptr(self) -> int:
+        return lib().ftmoe_lru_slot_of(self._h)
+
+    def slot_of(self, stream=None) -> torch.Tensor:
+        """A copy of the slot_of table [L, E] (device)."""
+        out = torch.empty(self.L, self.E, dtype=torch.int32, device="cuda")
+        _check(lib().ftmoe_lru_copy_slot_of(self._h, _ptr(out), _stream(stream)), "ftmoe_lru_copy_slot_of")
+        return out
+
+    def step(self, layer, ids, hit, slot, evicted, counters, stream=None):
+        B, k = ids.shape
+        _check(lib().ftmoe_slot_lru(self._h, layer, _ptr(ids), B, k, _ptr(hit), _ptr(slot), _ptr(evicted),
+                                    _ptr(counters), _stream(stream)), "ftmoe_slot_lru")
+
+    def replay(self, trace, hit, slot, evicted, counters, stream=None):
+        steps, L, B, k = trace.shape
+        if L != self.L:
+            raise FtmoeError("trace layer count differs from the handle's")
+        _check(lib().ftmoe_slot_lru_replay(self._h, _ptr(trace), steps, B, k, _ptr(hit), _ptr(slot), _ptr(evicted),
+                                           hit.numel(), _ptr(counters), _stream(stream)), "ftmoe_slot_lru_replay")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().ftmoe_lru_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

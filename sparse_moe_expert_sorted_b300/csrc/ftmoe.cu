@@ -1,0 +1,473 @@
+// ftmoe C ABI: argument checks, workspace layout and kernel launches.
+// All kernels live in this one translation unit (they share the device error word).
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+#include "combine.cuh"
+#include "ffn_stream.cuh"
+#include "lru.cuh"
+#include "permute.cuh"
+#include "route.cuh"
+
+using namespace ftmoe;
+
+struct ftmoe_lru {
+  LruState st;
+  void* mem;
+  int device;
+};
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  if (!g_sms[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = v > 0 ? v : 148;
+  }
+  return g_sms[dev];
+}
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Launch with programmatic stream serialisation: the kernel may start while the
+// previous kernel on the stream drains; it calls griddepcontrol.wait before
+// touching dependent memory.
+template <typename... KArgs, typename... Args>
+ftmoe_status launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                    Args... args) {
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+      return FTMOE_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  return err == cudaSuccess ? FTMOE_OK : FTMOE_ERR_CUDA;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool desc_ok(const ftmoe_layer_desc* d) {
+  if (!d) return false;
+  if (d->E < 1 || d->E > 1024) return false;
+  if (d->k < 1 || d->k > 32 || d->k > d->E) return false;
+  if (d->d < 256 || d->d % 256) return false;
+  if (d->ffn < 128 || d->ffn % 128) return false;
+  if (d->fmt < FTMOE_BF16 || d->fmt > FTMOE_FP8_B128) return false;
+  if (d->renorm != 0 && d->renorm != 1) return false;
+  if (d->fmt == FTMOE_FP8_B128 && (d->d % 128 || d->ffn % 128)) return false;
+  return true;
+}
+
+constexpr int kMaxT = 1 << 20;
+
+inline int cdiv(long long a, long long b) { return int((a + b - 1) / b); }
+
+// --- workspace layouts -------------------------------------------------------
+size_t route_ws(const ftmoe_layer_desc* d, int T, bool own_logits) {
+  return kWsHeader + (own_logits ? align256(size_t(T) * d->E * sizeof(float)) : 0);
+}
+size_t permute_ws(const ftmoe_layer_desc* d, int T) {
+  const int P = T * d->k;
+  const int nch = cdiv(P, kPermChunk);
+  return kWsHeader + (nch > 1 ? align256(size_t(nch) * d->E * sizeof(int)) : 0);
+}
+size_t ffn_ws(const ftmoe_layer_desc* d, int T) {
+  const size_t P = size_t(T) * d->k;
+  return kWsHeader + align256(P * d->ffn * sizeof(float));
+}
+
+ftmoe_status route_impl(const ftmoe_layer_desc* d, const uint16_t* x, const uint16_t* wr, const float* bias, int T,
+                        int32_t* ids, float* w, float* logits, void* ws, cudaStream_t st) {
+  RouteArgs a;
+  a.x = x;
+  a.wr = wr;
+  a.bias = bias;
+  a.T = T;
+  a.E = d->E;
+  a.d = d->d;
+  a.k = d->k;
+  a.renorm = d->renorm;
+  a.logits = logits ? logits : reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+  a.ids = ids;
+  a.w = w;
+  a.counter = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kWsCounterRoute);
+  const int fused = T <= kSelectSmallT;
+  const int sms = num_sms();
+  ftmoe_status s;
+  dim3 blk(kRouteWarps * 32);
+  if (T == 1) {
+    const int items = d->E;
+    s = launch(route_logits_kernel<1, 1>, dim3(std::min(cdiv(items, kRouteWarps), sms * 8)), blk, 0, st, a, fused);
+  } else if (T <= 64) {
+    const int items = d->E * cdiv(T, 8);
+    s = launch(route_logits_kernel<1, 8>, dim3(std::min(cdiv(items, kRouteWarps), sms * 8)), blk, 0, st, a, fused);
+  } else {
+    const long long items = (long long)cdiv(d->E, 4) * cdiv(T, 8);
+    s = launch(route_logits_kernel<4, 8>, dim3((unsigned)std::min<long long>(cdiv(items, kRouteWarps), sms * 8)),
+               blk, 0, st, a, fused);
+  }
+  if (s != FTMOE_OK || fused) return s;
+  return launch(route_select_kernel, dim3(std::min(cdiv(T, kRouteWarps), sms * 8)), blk, 0, st, a);
+}
+
+ftmoe_status permute_impl(const ftmoe_layer_desc* d, const int32_t* ids, int T, int32_t* off, int32_t* sp,
+                          int32_t* pp, void* ws, cudaStream_t st) {
+  const int P = T * d->k;
+  const int nch = cdiv(P, kPermChunk);
+  const int E = d->E;
+  if (nch == 1)
+    return launch(permute_rank_kernel, dim3(1), dim3(kPermChunk), permute_rank_smem(E), st, ids, P, E,
+                  (const int32_t*)nullptr, 1, off, sp, pp);
+  int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kWsHeader);
+  ftmoe_status s = launch(permute_hist_kernel, dim3(nch), dim3(kPermChunk), size_t(E) * sizeof(int), st, ids, P, E, hist);
+  if (s != FTMOE_OK) return s;
+  return launch(permute_rank_kernel, dim3(nch), dim3(kPermChunk), permute_rank_smem(E), st, ids, P, E,
+                (const int32_t*)hist, nch, off, sp, pp);
+}
+
+template <int FMT>
+ftmoe_status ffn_stream_launch(const FfnArgs& a, int P, cudaStream_t st) {
+  const int sms = num_sms();
+  const long long tiles = cdiv(P, kTokTile) + std::min(a.E, P);
+  const long long items_gu = tiles * a.f, items_d = tiles * a.d;
+  const int cap = sms * 16;
+  dim3 blk(kFfnWarps * 32);
+  ftmoe_status s = launch(ffn_gate_up_kernel<FMT>, dim3((unsigned)std::min<long long>(cdiv(items_gu, kFfnWarps), cap)),
+                          blk, 0, st, a);
+  if (s != FTMOE_OK) return s;
+  return launch(ffn_down_kernel<FMT>, dim3((unsigned)std::min<long long>(cdiv(items_d, kFfnWarps), cap)), blk, 0, st, a);
+}
+
+bool weights_ok(const ftmoe_layer_desc* d, const ftmoe_weights* w) {
+  if (!w) return false;
+  if (w->fmt != d->fmt || w->d != d->d || w->ffn != d->ffn || w->C < 1) return false;
+  if (!w->gate || !w->up || !w->down) return false;
+  if (!aligned16(w->gate) || !aligned16(w->up) || !aligned16(w->down)) return false;
+  if (d->fmt != FTMOE_BF16) {
+    if (!w->gate_scale || !w->up_scale || !w->down_scale) return false;
+    if (!aligned16(w->gate_scale) || !aligned16(w->up_scale) || !aligned16(w->down_scale)) return false;
+  }
+  if (d->fmt == FTMOE_NVFP4 && !w->tensor_scale) return false;
+  return true;
+}
+
+ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of, const uint16_t* x,
+                      int T, const int32_t* off, const int32_t* sp, const float* topk_w, float* y_or_out, void* ws,
+                      cudaStream_t st) {
+  FfnArgs a;
+  a.E = d->E;
+  a.k = d->k;
+  a.d = d->d;
+  a.f = d->ffn;
+  a.C = w->C;
+  a.gate = static_cast<const uint8_t*>(w->gate);
+  a.up = static_cast<const uint8_t*>(w->up);
+  a.down = static_cast<const uint8_t*>(w->down);
+  a.gate_s = static_cast<const uint8_t*>(w->gate_scale);
+  a.up_s = static_cast<const uint8_t*>(w->up_scale);
+  a.down_s = static_cast<const uint8_t*>(w->down_scale);
+  a.tscale = d->fmt == FTMOE_NVFP4 ? w->tensor_scale : nullptr;
+  a.slot_of = slot_of;
+  a.x = x;
+  a.T = T;
+  a.offsets = off;
+  a.sorted_pair = sp;
+  a.topk_w = topk_w;
+  a.y_or_out = y_or_out;
+  a.h = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+  const int P = T * d->k;
+  switch (d->fmt) {
+    case FTMOE_BF16: return ffn_stream_launch<FTMOE_BF16>(a, P, st);
+    case FTMOE_NVFP4: return ffn_stream_launch<FTMOE_NVFP4>(a, P, st);
+    case FTMOE_MXFP4: return ffn_stream_launch<FTMOE_MXFP4>(a, P, st);
+    case FTMOE_FP8_B128: return ffn_stream_launch<FTMOE_FP8_B128>(a, P, st);
+  }
+  return FTMOE_ERR_UNSUPPORTED;
+}
+
+ftmoe_status combine_impl(const ftmoe_layer_desc* d, int T, const float* y, const int32_t* pp, const float* w,
+                          const int32_t* ids, const int32_t* slot_of, const float* pb, float* of, uint16_t* ob,
+                          cudaStream_t st) {
+  CombineArgs a;
+  a.T = T;
+  a.k = d->k;
+  a.d = d->d;
+  a.E = d->E;
+  a.y = y;
+  a.pair_pos = pp;
+  a.topk_w = w;
+  a.topk_ids = ids;
+  a.slot_of = slot_of;
+  a.partial_b = pb;
+  a.out_f32 = of;
+  a.out_bf16 = ob;
+  const long long n = (long long)T * (d->d / 4);
+  return launch(combine_kernel, dim3((unsigned)std::min<long long>(cdiv(n, 256), num_sms() * 8)), dim3(256), 0, st, a);
+}
+
+}  // namespace
+
+// =============================================================================
+extern "C" {
+
+int ftmoe_version(void) { return 100; }
+
+const char* ftmoe_status_string(ftmoe_status s) {
+  switch (s) {
+    case FTMOE_OK: return "ok";
+    case FTMOE_ERR_INVALID_ARG: return "invalid argument";
+    case FTMOE_ERR_UNSUPPORTED: return "unsupported";
+    case FTMOE_ERR_CUDA: return "CUDA error";
+    case FTMOE_ERR_WORKSPACE: return "workspace too small";
+    case FTMOE_ERR_TIMEOUT: return "device wait timed out";
+    case FTMOE_ERR_DEVICE_CHECK: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+ftmoe_status ftmoe_get_device_error(int* code, void* stream) {
+  if (!code) return FTMOE_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  int v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_dev_err, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return FTMOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FTMOE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbolAsync(g_dev_err, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return FTMOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FTMOE_ERR_CUDA;
+  *code = v;
+  return FTMOE_OK;
+}
+
+size_t ftmoe_route_workspace_size(const ftmoe_layer_desc* d, int T) {
+  if (!desc_ok(d) || T < 1) return 0;
+  return route_ws(d, T, true);
+}
+
+ftmoe_status ftmoe_route(const ftmoe_layer_desc* d, const uint16_t* x, const uint16_t* wr, const float* bias, int T,
+                         int32_t* ids, float* w, float* logits, void* ws, size_t ws_bytes, void* stream) {
+  if (!desc_ok(d) || T < 1 || T > kMaxT || !x || !wr || !ids || !w || !ws) return FTMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(wr)) return FTMOE_ERR_INVALID_ARG;
+  if (ws_bytes < route_ws(d, T, logits == nullptr)) return FTMOE_ERR_WORKSPACE;
+  return route_impl(d, x, wr, bias, T, ids, w, logits, ws, as_stream(stream));
+}
+
+size_t ftmoe_permute_workspace_size(const ftmoe_layer_desc* d, int T) {
+  if (!desc_ok(d) || T < 1) return 0;
+  return permute_ws(d, T);
+}
+
+ftmoe_status ftmoe_permute(const ftmoe_layer_desc* d, const int32_t* ids, int T, int32_t* off, int32_t* sp,
+                           int32_t* pp, void* ws, size_t ws_bytes, void* stream) {
+  if (!desc_ok(d) || T < 1 || T > kMaxT || !ids || !off || !sp || !pp || !ws) return FTMOE_ERR_INVALID_ARG;
+  if (ws_bytes < permute_ws(d, T)) return FTMOE_ERR_WORKSPACE;
+  return permute_impl(d, ids, T, off, sp, pp, ws, as_stream(stream));
+}
+
+size_t ftmoe_expert_ffn_workspace_size(const ftmoe_layer_desc* d, int T) {
+  if (!desc_ok(d) || T < 1) return 0;
+  return ffn_ws(d, T);
+}
+
+int ftmoe_expert_ffn_path(const ftmoe_layer_desc* d, int T) {
+  if (!desc_ok(d) || T < 1) return -1;
+  return 0;
+}
+
+ftmoe_status ftmoe_expert_ffn(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of,
+                              const uint16_t* x, int T, const int32_t* off, const int32_t* sp, const float* topk_w,
+                              float* y_or_out, void* ws, size_t ws_bytes, void* stream) {
+  if (!desc_ok(d) || T < 1 || T > kMaxT || !x || !off || !sp || !y_or_out || !ws) return FTMOE_ERR_INVALID_ARG;
+  if (!weights_ok(d, w) || !aligned16(x) || !aligned16(y_or_out)) return FTMOE_ERR_INVALID_ARG;
+  if (ws_bytes < ffn_ws(d, T)) return FTMOE_ERR_WORKSPACE;
+  return ffn_impl(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, as_stream(stream));
+}
+
+ftmoe_status ftmoe_combine(const ftmoe_layer_desc* d, int T, const float* y, const int32_t* pp, const float* w,
+                           const int32_t* ids, const int32_t* slot_of, const float* pb, float* of, uint16_t* ob,
+                           void* stream) {
+  if (!desc_ok(d) || T < 1 || T > kMaxT || (!of && !ob)) return FTMOE_ERR_INVALID_ARG;
+  if (y && (!pp || !w)) return FTMOE_ERR_INVALID_ARG;
+  if (y && slot_of && !ids) return FTMOE_ERR_INVALID_ARG;
+  if ((y && !aligned16(y)) || (pb && !aligned16(pb)) || (of && !aligned16(of))) return FTMOE_ERR_INVALID_ARG;
+  if (ob && (reinterpret_cast<uintptr_t>(ob) & 7u)) return FTMOE_ERR_INVALID_ARG;
+  return combine_impl(d, T, y, pp, w, ids, slot_of, pb, of, ob, as_stream(stream));
+}
+
+// --- LRU ---------------------------------------------------------------------
+ftmoe_status ftmoe_lru_create(int L, int E, int C, ftmoe_lru** out) {
+  if (!out || L < 1 || E < 1 || C < 1) return FTMOE_ERR_INVALID_ARG;
+  if (lru_smem_bytes(L, E, C) > 200 * 1024) return FTMOE_ERR_UNSUPPORTED;
+  ftmoe_lru* h = new (std::nothrow) ftmoe_lru();
+  if (!h) return FTMOE_ERR_CUDA;
+  const size_t n_int = size_t(L) * E + 3 * size_t(C) + 4;
+  const size_t bytes = align256(n_int * sizeof(int32_t)) + 2 * sizeof(long long);
+  if (cudaMalloc(&h->mem, bytes) != cudaSuccess) {
+    delete h;
+    return FTMOE_ERR_CUDA;
+  }
+  cudaGetDevice(&h->device);
+  int32_t* p = static_cast<int32_t*>(h->mem);
+  h->st.slot_of = p;
+  h->st.key_of = p + size_t(L) * E;
+  h->st.prv = h->st.key_of + C;
+  h->st.nxt = h->st.prv + C;
+  h->st.meta = h->st.nxt + C;
+  h->st.totals = reinterpret_cast<long long*>(static_cast<char*>(h->mem) + align256(n_int * sizeof(int32_t)));
+  h->st.L = L;
+  h->st.E = E;
+  h->st.C = C;
+  ftmoe_status s = ftmoe_lru_reset(h, nullptr);
+  if (s == FTMOE_OK && cudaStreamSynchronize(nullptr) != cudaSuccess) s = FTMOE_ERR_CUDA;
+  if (s != FTMOE_OK) {
+    cudaFree(h->mem);
+    delete h;
+    return s;
+  }
+  *out = h;
+  return FTMOE_OK;
+}
+
+ftmoe_status ftmoe_lru_reset(ftmoe_lru* h, void* stream) {
+  if (!h) return FTMOE_ERR_INVALID_ARG;
+  const int n = std::max(h->st.L * h->st.E, h->st.C);
+  return launch(lru_reset_kernel, dim3(std::min(cdiv(n, 256), 64)), dim3(256), 0, as_stream(stream), h->st);
+}
+
+ftmoe_status ftmoe_lru_destroy(ftmoe_lru* h) {
+  if (!h) return FTMOE_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  cudaError_t e = cudaFree(h->mem);
+  delete h;
+  return e == cudaSuccess ? FTMOE_OK : FTMOE_ERR_CUDA;
+}
+
+const int32_t* ftmoe_lru_slot_of(const ftmoe_lru* h) { return h ? h->st.slot_of : nullptr; }
+
+ftmoe_status ftmoe_lru_copy_slot_of(const ftmoe_lru* h, int32_t* dst, void* stream) {
+  if (!h || !dst) return FTMOE_ERR_INVALID_ARG;
+  const size_t n = size_t(h->st.L) * h->st.E * sizeof(int32_t);
+  return cudaMemcpyAsync(dst, h->st.slot_of, n, cudaMemcpyDeviceToDevice, as_stream(stream)) == cudaSuccess
+             ? FTMOE_OK
+             : FTMOE_ERR_CUDA;
+}
+
+ftmoe_status ftmoe_slot_lru(ftmoe_lru* h, int layer, const int32_t* ids, int B, int k, uint8_t* hit, int32_t* slot,
+                            int32_t* ev, int64_t* counters, void* stream) {
+  if (!h || !ids || !hit || !slot || !ev || B < 1 || k < 1) return FTMOE_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->st.L) return FTMOE_ERR_INVALID_ARG;
+  const long long cap = std::min<long long>((long long)B * k, h->st.E);
+  return launch(lru_kernel, dim3(1), dim3(kLruThreads), lru_smem_bytes(h->st.L, h->st.E, h->st.C),
+                as_stream(stream), h->st, ids, 1, B * k, layer, 0, hit, slot, ev, cap,
+                reinterpret_cast<long long*>(counters));
+}
+
+ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* h, const int32_t* trace, int steps, int B, int k, uint8_t* hit,
+                                   int32_t* slot, int32_t* ev, int64_t capacity, int64_t* counters, void* stream) {
+  if (!h || !trace || !hit || !slot || !ev || steps < 1 || B < 1 || k < 1 || capacity < 0) return FTMOE_ERR_INVALID_ARG;
+  return launch(lru_kernel, dim3(1), dim3(kLruThreads), lru_smem_bytes(h->st.L, h->st.E, h->st.C),
+                as_stream(stream), h->st, trace, steps * h->st.L, B * k, 0, 1, hit, slot, ev, (long long)capacity,
+                reinterpret_cast<long long*>(counters));
+}
+
+// --- whole layer -------------------------------------------------------------
+// Workspace: header | ids | w | offsets | sorted_pair | pair_pos | y | (route/permute/ffn scratch, shared)
+namespace {
+struct LayerWs {
+  size_t ids, w, off, sp, pp, y, scratch, total;
+};
+LayerWs layer_ws(const ftmoe_layer_desc* d, int T) {
+  LayerWs L;
+  const size_t P = size_t(T) * d->k;
+  size_t o = kWsHeader;
+  L.ids = o; o += align256(P * 4);
+  L.w = o; o += align256(P * 4);
+  L.off = o; o += align256(size_t(d->E + 1) * 4);
+  L.sp = o; o += align256(P * 4);
+  L.pp = o; o += align256(P * 4);
+  L.y = o; o += align256(P * d->d * sizeof(float));
+  L.scratch = o;
+  // scratch regions reuse the same bytes after the header, so offset them by the header size
+  const size_t sr = route_ws(d, T, true) - kWsHeader;
+  const size_t sq = permute_ws(d, T) - kWsHeader;
+  const size_t sf = ffn_ws(d, T) - kWsHeader;
+  o += std::max(sr, std::max(sq, sf));
+  L.total = o;
+  return L;
+}
+}  // namespace
+
+size_t ftmoe_layer_workspace_size(const ftmoe_layer_desc* d, int T) {
+  if (!desc_ok(d) || T < 1) return 0;
+  return layer_ws(d, T).total;
+}
+
+ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of,
+                                 const uint16_t* x, const uint16_t* wr, const float* bias, int T, int32_t* ids,
+                                 float* tw, float* out_f32, uint16_t* out_bf16, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  if (!desc_ok(d) || T < 1 || T > kMaxT || !x || !wr || !out_f32 || !ws) return FTMOE_ERR_INVALID_ARG;
+  if ((ids == nullptr) != (tw == nullptr)) return FTMOE_ERR_INVALID_ARG;
+  if (!weights_ok(d, w) || !aligned16(x) || !aligned16(wr) || !aligned16(out_f32)) return FTMOE_ERR_INVALID_ARG;
+  if (out_bf16 && (reinterpret_cast<uintptr_t>(out_bf16) & 7u)) return FTMOE_ERR_INVALID_ARG;
+  const LayerWs L = layer_ws(d, T);
+  if (ws_bytes < L.total) return FTMOE_ERR_WORKSPACE;
+  char* base = static_cast<char*>(ws);
+  cudaStream_t st = as_stream(stream);
+  int32_t* ids_ = ids ? ids : reinterpret_cast<int32_t*>(base + L.ids);
+  float* w_ = tw ? tw : reinterpret_cast<float*>(base + L.w);
+  int32_t* off = reinterpret_cast<int32_t*>(base + L.off);
+  int32_t* sp = reinterpret_cast<int32_t*>(base + L.sp);
+  int32_t* pp = reinterpret_cast<int32_t*>(base + L.pp);
+  float* y = reinterpret_cast<float*>(base + L.y);
+  // The steps run in order on one stream, so they share one scratch region:
+  // router logits, then the permutation histogram, then h.  Counters stay in
+  // the caller's zero header at `base`.  The FFN addresses its buffer at
+  // ws + kWsHeader, so it gets a view that ends its header where scratch starts.
+  char* view = base + L.scratch - kWsHeader;
+  ftmoe_status s;
+  // route: logits go to the scratch region (the view's buffer area)
+  s = route_impl(d, x, wr, bias, T, ids_, w_, reinterpret_cast<float*>(base + L.scratch), base, st);
+  if (s != FTMOE_OK) return s;
+  // permute: its histogram lives in the scratch region too
+  {
+    const int P = T * d->k;
+    const int nch = cdiv(P, kPermChunk);
+    if (nch == 1) {
+      s = launch(permute_rank_kernel, dim3(1), dim3(kPermChunk), permute_rank_smem(d->E), st, (const int32_t*)ids_, P,
+                 d->E, (const int32_t*)nullptr, 1, off, sp, pp);
+    } else {
+      int32_t* hist = reinterpret_cast<int32_t*>(base + L.scratch);
+      s = launch(permute_hist_kernel, dim3(nch), dim3(kPermChunk), size_t(d->E) * sizeof(int), st,
+                 (const int32_t*)ids_, P, d->E, hist);
+      if (s == FTMOE_OK)
+        s = launch(permute_rank_kernel, dim3(nch), dim3(kPermChunk), permute_rank_smem(d->E), st,
+                   (const int32_t*)ids_, P, d->E, (const int32_t*)hist, nch, off, sp, pp);
+    }
+  }
+  if (s != FTMOE_OK) return s;
+  s = ffn_impl(d, w, slot_of, x, T, off, sp, nullptr, y, view, st);
+  if (s != FTMOE_OK) return s;
+  return combine_impl(d, T, y, pp, w_, ids_, slot_of, nullptr, out_f32, out_bf16, st);
+}
+
+}  // extern "C"

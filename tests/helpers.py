@@ -27,3 +27,38 @@ def rel_l2(a, b):
     b = np.asarray(b, np.float64)
     den = np.linalg.norm(b)
     return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
+
+
+class LazySlots:
+    """Slot-indexed view of a (device) tensor; slot s is copied to host on first use."""
+
+    def __init__(self, t):
+        self.t = t
+        self.cache = {}
+
+    def __getitem__(self, s):
+        s = int(s)
+        if s not in self.cache:
+            self.cache[s] = self.t[s].detach().cpu().numpy()
+        return self.cache[s]
+
+
+def weights_lazy(W):
+    """The oracle's weight dict over device tensors, fetching slots on demand."""
+    import torch
+    out = dict(fmt=W.fmt, d=W.d, f=W.f)
+    for name in ("gate", "up", "down"):
+        t = getattr(W, name)
+        out[name] = _Bf16Slots(t) if t.dtype == torch.bfloat16 else LazySlots(t)
+        s = getattr(W, name + "_s")
+        out[name + "_s"] = None if s is None else LazySlots(s)
+    out["glob"] = W.glob.detach().cpu().numpy()
+    return out
+
+
+class _Bf16Slots(LazySlots):
+    def __getitem__(self, s):
+        s = int(s)
+        if s not in self.cache:
+            self.cache[s] = bf16_bits(self.t[s])
+        return self.cache[s]
