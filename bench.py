@@ -64,6 +64,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="layer copies to cycle (decode workloads; default 16)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU baseline sample")
     return ap.parse_args()
 
@@ -204,6 +205,8 @@ def bench_ours(args, rank, ws):
     import sparse_moe_expert_sorted_b300 as ft
     ft.lib()  # fails loudly if the library is missing
     wl, T, n_layers = WORKLOADS[args.workload]
+    if args.layers and not args.workload.startswith("stack"):
+        n_layers = args.layers
     L = wl.layer
     dev = "cuda"
     dsc = ft.desc(L.E, L.k, L.d, L.f, L.fmt, L.renorm)
@@ -267,8 +270,9 @@ def bench_ours(args, rank, ws):
     with torch.cuda.graph(graph, stream=main):
         for i in range(K):
             step(i)
-    for _ in range(max(3, args.warmup // max(1, K) + 1)):
-        graph.replay()
+    with torch.cuda.stream(main):     # replay() launches on the current stream
+        for _ in range(max(3, args.warmup // max(1, K) + 1)):
+            graph.replay()
     torch.cuda.synchronize()
 
     clocks = ClockSampler(torch.cuda.current_device())
@@ -278,9 +282,10 @@ def bench_ours(args, rank, ws):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(main)
-    graph.replay()
-    t1.record(main)
+    with torch.cuda.stream(main):
+        t0.record(main)
+        graph.replay()
+        t1.record(main)
     t1.synchronize()
     torch.cuda.synchronize()
     barrier(ws)
@@ -322,9 +327,9 @@ def bench_ours(args, rank, ws):
             sev[i].record(main)
             ft.expert_ffn(dsc, structs[li], None, x, r_off, r_sp, None, y, ws_f, main)
             eev[i].record(main)
-    g2.replay()
-    torch.cuda.synchronize()
-    g2.replay()
+    with torch.cuda.stream(main):
+        g2.replay()
+        g2.replay()
     torch.cuda.synchronize()
     ffn_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(sev, eev)]))
     eb = expert_bytes(wl)
@@ -407,7 +412,6 @@ def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
 def oracle_rate(workload: str, budget_s: float, max_steps: int | None = None):
     """Oracle tokens/s on a bounded sample of the workload (host cores)."""
     from oracle import ffn as OF
-    from threadpoolctl import threadpool_info
     wl, T, n_layers = WORKLOADS[workload]
     L = wl.layer
     stack = workload.startswith("stack")
@@ -436,10 +440,25 @@ def oracle_rate(workload: str, budget_s: float, max_steps: int | None = None):
         el = time.perf_counter() - t0
         if el >= budget_s or (max_steps and steps >= max_steps):
             break
-    threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    threads = blas_threads()
     sample = (f"{steps} oracle step(s) of {sample_T} token(s)" + (" x 8 layers" if stack else "") +
               f" ({'the full batch' if sample_T == T else f'a {sample_T}-token sample of the {T}-token chunk'})")
     return done_tokens / el, threads, sample, el
+
+
+def blas_threads() -> int:
+    """Threads numpy's BLAS uses (the oracle's matmuls); else the usable cores."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except ImportError:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
 
 
 def bench_reference(args, rank, ws):
