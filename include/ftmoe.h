@@ -129,6 +129,28 @@ ftmoe_status ftmoe_route(const ftmoe_layer_desc* desc, const uint16_t* x, const 
                          void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ftmoe_route_noalloc - ftmoe_route for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a deployment convenience of this library.
+ * Some callers cannot call cudaMalloc or own a workspace.  Examples: code running
+ * under a memory pool that already owns the whole device budget, and code inside
+ * another library's callback where an allocation could fail or synchronise the
+ * device at an unpredictable moment.  This variant takes inputs and outputs only,
+ * exactly as ftmoe_route does with logits = NULL.  Its scratch (a counter and the
+ * [T][E] fp32 logits) is a fixed array inside the library that every GPU loading
+ * it holds until the process exits; it allocates nothing and calls no allocating
+ * routine.
+ *   - T * E must not exceed FTMOE_NOALLOC_MAX_LOGITS (1 MiB of logits); larger
+ *     requests return FTMOE_ERR_WORKSPACE.
+ *   - The first call on a device looks up the array's device address.  Make that
+ *     first call before capturing a stream.
+ *   - All calls share the one array: calls that can overlap on the GPU (other
+ *     streams, other host threads) race and must be serialised by the caller.
+ * ------------------------------------------------------------------------- */
+#define FTMOE_NOALLOC_MAX_LOGITS 262144
+ftmoe_status ftmoe_route_noalloc(const ftmoe_layer_desc* desc, const uint16_t* x, const uint16_t* w_router,
+                                 const float* logit_bias, int T, int32_t* topk_ids, float* topk_w, void* stream);
+
+/* ---------------------------------------------------------------------------
  * a2  ftmoe_permute - stable expert-sorted permutation of the P = T*k pairs.
  * The pages do not describe it.  It is what computing each selected expert
  * once over a batch needs (banandre.com, section "Sparsity Is a Lie").

@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libftmoe.so")
 
 # Symbols declared in include/ftmoe.h (checked by the ABI test).
 EXPORTS = [
-    "ftmoe_route_workspace_size", "ftmoe_route", "ftmoe_permute_workspace_size", "ftmoe_permute",
+    "ftmoe_route_workspace_size", "ftmoe_route", "ftmoe_route_noalloc", "ftmoe_permute_workspace_size", "ftmoe_permute",
     "ftmoe_expert_ffn_workspace_size", "ftmoe_expert_ffn_path", "ftmoe_expert_ffn", "ftmoe_combine", "ftmoe_lru_create", "ftmoe_lru_reset",
     "ftmoe_lru_destroy", "ftmoe_lru_slot_of", "ftmoe_lru_copy_slot_of", "ftmoe_slot_lru", "ftmoe_slot_lru_replay",
     "ftmoe_layer_workspace_size", "ftmoe_layer_forward", "ftmoe_status_string", "ftmoe_get_device_error",
@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
     sig = {
         "ftmoe_route_workspace_size": (_SZ, [_P, _I]),
         "ftmoe_route": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
+        "ftmoe_route_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _P, _P]),
         "ftmoe_permute_workspace_size": (_SZ, [_P, _I]),
         "ftmoe_permute": (_I, [_P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
         "ftmoe_expert_ffn_workspace_size": (_SZ, [_P, _I]),
@@ -157,6 +158,14 @@ def route(dsc, x, w_router, bias, ids, w, logits, ws, stream=None):
     T = x.shape[0]
     _check(lib().ftmoe_route(ctypes.byref(dsc), _ptr(x), _ptr(w_router), _ptr(bias), T, _ptr(ids), _ptr(w),
                              _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)), "ftmoe_route")
+
+
+def route_noalloc(dsc, x, w_router, bias, ids, w, stream=None):
+    """ftmoe_route without a workspace: for callers that cannot allocate device memory.
+    Calls sharing the library's fixed scratch must not overlap on the GPU."""
+    T = x.shape[0]
+    _check(lib().ftmoe_route_noalloc(ctypes.byref(dsc), _ptr(x), _ptr(w_router), _ptr(bias), T, _ptr(ids), _ptr(w),
+                                     _stream(stream)), "ftmoe_route_noalloc")
 
 
 def permute_workspace_size(dsc: LayerDesc, T: int) -> int:

@@ -2,6 +2,7 @@
 // All kernels live in this one translation unit (they share the device error word).
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "common.cuh"
@@ -471,3 +472,50 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
 }
 
 }  // extern "C"
+
+// =============================================================================
+// ftmoe_route_noalloc: the router for callers that cannot allocate device memory.
+//
+// Its scratch (the completion counter and the [T][E] fp32 logits) lives in one
+// fixed array that every GPU loading this library holds until the process
+// exits.  Host code must not hand the array's name to a kernel: on the host it
+// is only a stand-in symbol.  The device address comes from
+// cudaGetSymbolAddress, taken once per device (with that device current) on
+// the first call there.  Every call shares the array, so calls that overlap on
+// the GPU race; each call zeroes the counter before its kernels run.
+// =============================================================================
+static __device__ __align__(256) unsigned char g_route_noalloc_scratch[FTMOE_WS_ZERO_BYTES +
+                                                                       FTMOE_NOALLOC_MAX_LOGITS * sizeof(float)];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices];
+
+// Device address of the fixed scratch array on the current device (set up once per device).
+ftmoe_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FTMOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FTMOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_noalloc_scratch) != cudaSuccess || !p) return FTMOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return FTMOE_OK;
+}
+}  // namespace
+
+extern "C" ftmoe_status ftmoe_route_noalloc(const ftmoe_layer_desc* d, const uint16_t* x, const uint16_t* wr,
+                                            const float* bias, int T, int32_t* ids, float* w, void* stream) {
+  if (!desc_ok(d) || T < 1 || T > kMaxT || !x || !wr || !ids || !w) return FTMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(wr)) return FTMOE_ERR_INVALID_ARG;
+  if (size_t(T) * size_t(d->E) > size_t(FTMOE_NOALLOC_MAX_LOGITS)) return FTMOE_ERR_WORKSPACE;
+  void* ws = nullptr;
+  const ftmoe_status s = noalloc_scratch(&ws);
+  if (s != FTMOE_OK) return s;
+  cudaStream_t st = as_stream(stream);
+  if (cudaMemsetAsync(ws, 0, FTMOE_WS_ZERO_BYTES, st) != cudaSuccess) return FTMOE_ERR_CUDA;
+  return route_impl(d, x, wr, bias, T, ids, w, nullptr, ws, st);
+}
