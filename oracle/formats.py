@@ -162,7 +162,8 @@ def quant_act_nvfp4(v: np.ndarray):
     For each block of 16 consecutive elements:
         s_code = E4M3_rn_satfinite(amax / 6)   (IEEE fp32 division)
         s      = value of s_code
-        q      = E2M1_rn_satfinite(v / s)       (IEEE fp32 division), or +-0 if s == 0
+        q      = E2M1_rn_satfinite(v / s)       (IEEE fp32 division), or a zero
+                 with v's sign bit if s == 0 (so -0.0 gives the code of -0)
     The tensor-level scale is 1.
     """
     v = np.asarray(v, np.float32)
@@ -173,7 +174,7 @@ def quant_act_nvfp4(v: np.ndarray):
     s = E4M3_LUT[s_code].astype(np.float32)
     with np.errstate(divide="ignore", invalid="ignore"):
         ratio = blk / s[..., None]
-    ratio = np.where(s[..., None] > 0, ratio, np.float32(0.0) * np.sign(blk))
+    ratio = np.where(s[..., None] > 0, ratio, np.copysign(np.float32(0.0), blk))
     q = e2m1_encode(ratio.astype(np.float32))
     return q.reshape(n, K), s_code
 
@@ -188,7 +189,8 @@ def quant_act_fp8(v: np.ndarray):
 
     Per row and per block of 128 consecutive elements:
         s = amax / 448                    (IEEE fp32 division)
-        q = E4M3_rn_satfinite(v / s)      (IEEE fp32 division), or +-0 if s == 0
+        q = E4M3_rn_satfinite(v / s)      (IEEE fp32 division), or a zero with
+                                          v's sign bit if s == 0
     """
     v = np.asarray(v, np.float32)
     n, K = v.shape
@@ -197,7 +199,7 @@ def quant_act_fp8(v: np.ndarray):
     s = (amax / np.float32(448.0)).astype(np.float32)
     with np.errstate(divide="ignore", invalid="ignore"):
         ratio = blk / s[..., None]
-    ratio = np.where(s[..., None] > 0, ratio, np.float32(0.0) * np.sign(blk))
+    ratio = np.where(s[..., None] > 0, ratio, np.copysign(np.float32(0.0), blk))
     q = e4m3_encode(ratio.astype(np.float32))
     return q.reshape(n, K), s
 
