@@ -99,7 +99,32 @@ typedef struct {
   const void* up_scale;
   const void* down_scale;
   const float* tensor_scale;
+  /* Scales repacked by ftmoe_prepare_weights for the tensor-core path, or NULL.
+   * Required when ftmoe_expert_ffn_path reports 1 for the call (NVFP4 prefill);
+   * the streaming path ignores it. */
+  const void* prepared;
 } ftmoe_weights;
+
+/* ---------------------------------------------------------------------------
+ * ftmoe_prepare_weights - repack the NVFP4 block scales of a slot arena for the
+ * tensor-core path.  Run once per arena (or after slots are refilled), outside
+ * any timed region; the codes themselves are used in place.
+ * Each MMA with K = 64 reads four scales per row from tensor memory.  The
+ * repacked layout holds, per 128 weight rows and per K = 64 step, the 512 bytes
+ * that one tcgen05.cp moves there: byte (r % 32) * 16 + (r / 32) * 4 + kb for
+ * row r of the 128 and 16-element block kb of the 64.
+ *   gate/up  [C][ffn/NH][d/64][A][512]: an N tile of NH gate rows then NH up rows
+ *            (NH = 96 if ffn % 96 == 0, else 64) in A = ceil(2*NH/128) blocks of
+ *            128 rows, zero past 2*NH rows
+ *   down     [C][d/128][ffn/64][512]
+ * weights->prepared is ignored here.  prep (device, prep_bytes from
+ * ftmoe_prepare_weights_size, 256-byte aligned) is written; it is then passed as
+ * weights->prepared.  Formats other than NVFP4 need nothing: size 0, and the call
+ * returns FTMOE_OK without work.
+ * ------------------------------------------------------------------------- */
+size_t ftmoe_prepare_weights_size(const ftmoe_layer_desc* desc, int C);
+ftmoe_status ftmoe_prepare_weights(const ftmoe_layer_desc* desc, const ftmoe_weights* weights, void* prep,
+                                   size_t prep_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * a1  ftmoe_route - router logits, top-k ids and their weights.
@@ -151,6 +176,23 @@ ftmoe_status ftmoe_route_noalloc(const ftmoe_layer_desc* desc, const uint16_t* x
                                  const float* logit_bias, int T, int32_t* topk_ids, float* topk_w, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * a3  ftmoe_quantize_act - the prefill activation quantiser on its own.
+ * The pages do not say how activations reach FP4 tensor cores.  The library's
+ * rule, applied inside ftmoe_expert_ffn's tensor-core path to the gathered rows
+ * of x and to h, is for each block of 16 consecutive elements of a row:
+ *   s_code = E4M3_rn_satfinite(amax / 6)            (IEEE fp32 division)
+ *   q      = E2M1_rn_satfinite(v / value(s_code))   (IEEE fp32 division),
+ *            or a zero of v's sign when the scale is 0
+ * with a tensor-level scale of 1.  This call applies it to x [T][d] (bf16) in
+ * token order:
+ *   codes   uint8 [T][d/2], element 2i in the low nibble of byte i
+ *   scales  uint8 [T][d/16], E4M3 codes
+ * Preconditions: 1 <= T <= 2^20, d % 256 == 0.
+ * ------------------------------------------------------------------------- */
+ftmoe_status ftmoe_quantize_act(const ftmoe_layer_desc* desc, const uint16_t* x, int T, uint8_t* codes,
+                                uint8_t* scales, void* stream);
+
+/* ---------------------------------------------------------------------------
  * a2  ftmoe_permute - stable expert-sorted permutation of the P = T*k pairs.
  * The pages do not describe it.  It is what computing each selected expert
  * once over a batch needs (banandre.com, section "Sparsity Is a Lie").
@@ -179,10 +221,18 @@ ftmoe_status ftmoe_permute(const ftmoe_layer_desc* desc, const int32_t* topk_ids
  *             sorted_pair[j]); rows of skipped experts are left untouched
  *             otherwise: fused combine.  y_or_out is out fp32 [T][d], and
  *             w[p] * y is ADDED into it (zero it first, or pass a partial to merge)
- * T at or above the prefill threshold runs the tensor-core path: activations
- * and h are quantised to NVFP4 (NVFP4 weights) or FP8 (FP8_B128 weights) by
- * the library's stated rule.  Smaller T runs the weight-only streaming path.
+ * Paths (ftmoe_expert_ffn_path tells which one a call takes):
+ *   0  weight-only streaming on CUDA cores: x and h stay fp32, no activation
+ *      quantisation.  Small T (decode), and every format the tensor-core path
+ *      does not cover.
+ *   1  NVFP4 weights, T >= FTMOE_PREFILL_MIN_T, d % 256 == 0, ffn % 256 == 0:
+ *      tcgen05 block-scaled tensor cores.  The gathered rows of x and h are
+ *      quantised to NVFP4 by the rule of ftmoe_quantize_act.  Needs
+ *      weights->prepared (FTMOE_ERR_INVALID_ARG without it).  With topk_w the
+ *      combine is fused (fp32 atomic adds, so the order of the k adds into
+ *      out varies between runs); without it y is written in sorted order.
  * ------------------------------------------------------------------------- */
+#define FTMOE_PREFILL_MIN_T 256
 size_t ftmoe_expert_ffn_workspace_size(const ftmoe_layer_desc* desc, int T);
 /* Which path ftmoe_expert_ffn takes for this layer and T: 0 = weight-only streaming
  * on CUDA cores (no activation quantisation), 1 = tensor cores with NVFP4

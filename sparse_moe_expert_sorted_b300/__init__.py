@@ -15,7 +15,8 @@ import torch
 
 __all__ = [
     "BF16", "NVFP4", "MXFP4", "FP8_B128", "LayerDesc", "FtmoeError", "lib", "route", "permute", "expert_ffn",
-    "combine", "layer_forward", "LRU", "weights_struct", "workspace", "get_device_error",
+    "combine", "layer_forward", "LRU", "weights_struct", "workspace", "get_device_error", "prepare_weights",
+    "quantize_act",
 ]
 
 BF16, NVFP4, MXFP4, FP8_B128 = 0, 1, 2, 3
@@ -27,6 +28,7 @@ LIB_PATH = os.path.join(_HERE, "libftmoe.so")
 # Symbols declared in include/ftmoe.h (checked by the ABI test).
 EXPORTS = [
     "ftmoe_route_workspace_size", "ftmoe_route", "ftmoe_route_noalloc", "ftmoe_permute_workspace_size", "ftmoe_permute",
+    "ftmoe_prepare_weights_size", "ftmoe_prepare_weights", "ftmoe_quantize_act",
     "ftmoe_expert_ffn_workspace_size", "ftmoe_expert_ffn_path", "ftmoe_expert_ffn", "ftmoe_combine", "ftmoe_lru_create", "ftmoe_lru_reset",
     "ftmoe_lru_destroy", "ftmoe_lru_slot_of", "ftmoe_lru_copy_slot_of", "ftmoe_slot_lru", "ftmoe_slot_lru_replay",
     "ftmoe_layer_workspace_size", "ftmoe_layer_forward", "ftmoe_status_string", "ftmoe_get_device_error",
@@ -47,7 +49,7 @@ class WeightsStruct(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int), ("C", ctypes.c_int), ("d", ctypes.c_int), ("ffn", ctypes.c_int),
                 ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p), ("down", ctypes.c_void_p),
                 ("gate_scale", ctypes.c_void_p), ("up_scale", ctypes.c_void_p), ("down_scale", ctypes.c_void_p),
-                ("tensor_scale", ctypes.c_void_p)]
+                ("tensor_scale", ctypes.c_void_p), ("prepared", ctypes.c_void_p)]
 
 
 _lib = None
@@ -68,6 +70,9 @@ def lib() -> ctypes.CDLL:
         "ftmoe_route_workspace_size": (_SZ, [_P, _I]),
         "ftmoe_route": (_I, [_P, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
         "ftmoe_route_noalloc": (_I, [_P, _P, _P, _P, _I, _P, _P, _P]),
+        "ftmoe_prepare_weights_size": (_SZ, [_P, _I]),
+        "ftmoe_prepare_weights": (_I, [_P, _P, _P, _SZ, _P]),
+        "ftmoe_quantize_act": (_I, [_P, _P, _I, _P, _P, _P]),
         "ftmoe_permute_workspace_size": (_SZ, [_P, _I]),
         "ftmoe_permute": (_I, [_P, _P, _I, _P, _P, _P, _P, _SZ, _P]),
         "ftmoe_expert_ffn_workspace_size": (_SZ, [_P, _I]),
@@ -143,11 +148,43 @@ class Weights:
     glob: torch.Tensor
 
 
-def weights_struct(W) -> WeightsStruct:
+def weights_struct(W, prepared=None) -> WeightsStruct:
     """ftmoe_weights view of an arena with attributes fmt, d, f, gate, up, down,
-    gate_s, up_s, down_s, glob (tensor scale [C, 3], NVFP4 only)."""
+    gate_s, up_s, down_s, glob (tensor scale [C, 3], NVFP4 only).  `prepared` is
+    the buffer filled by prepare_weights (needed by the NVFP4 tensor-core path);
+    by default the one prepare_weights attached to W, if any."""
+    if prepared is None:
+        prepared = getattr(W, "ftmoe_prepared", None)
     return WeightsStruct(W.fmt, W.gate.shape[0], W.d, W.f, _ptr(W.gate), _ptr(W.up), _ptr(W.down),
-                         _ptr(W.gate_s), _ptr(W.up_s), _ptr(W.down_s), _ptr(W.glob) if W.fmt == NVFP4 else None)
+                         _ptr(W.gate_s), _ptr(W.up_s), _ptr(W.down_s), _ptr(W.glob) if W.fmt == NVFP4 else None,
+                         _ptr(prepared))
+
+
+def prepare_weights_size(dsc: LayerDesc, C: int) -> int:
+    return lib().ftmoe_prepare_weights_size(ctypes.byref(dsc), C)
+
+
+def prepare_weights(dsc: LayerDesc, W, stream=None):
+    """Repack the arena's block scales for the tensor-core path (ftmoe_prepare_weights).
+    The buffer is attached to W (W.ftmoe_prepared) and returned; None when the
+    format needs no repack."""
+    C = W.gate.shape[0]
+    n = prepare_weights_size(dsc, C)
+    if n == 0:
+        return None
+    buf = torch.empty(n, dtype=torch.uint8, device=W.gate.device)
+    ws = weights_struct(W, prepared=0)
+    _check(lib().ftmoe_prepare_weights(ctypes.byref(dsc), ctypes.byref(ws), _ptr(buf), n, _stream(stream)),
+           "ftmoe_prepare_weights")
+    W.ftmoe_prepared = buf
+    return buf
+
+
+def quantize_act(dsc, x, codes, scales, stream=None):
+    """ftmoe_quantize_act: x [T, d] bf16 -> NVFP4 codes uint8 [T, d/2] + E4M3 scales uint8 [T, d/16]."""
+    T = x.shape[0]
+    _check(lib().ftmoe_quantize_act(ctypes.byref(dsc), _ptr(x), T, _ptr(codes), _ptr(scales), _stream(stream)),
+           "ftmoe_quantize_act")
 
 
 def route_workspace_size(dsc: LayerDesc, T: int) -> int:

@@ -10,6 +10,7 @@
 #include "ffn_stream.cuh"
 #include "lru.cuh"
 #include "permute.cuh"
+#include "prefill.cuh"
 #include "route.cuh"
 
 using namespace ftmoe;
@@ -90,9 +91,86 @@ size_t permute_ws(const ftmoe_layer_desc* d, int T) {
   const int nch = cdiv(P, kPermChunk);
   return kWsHeader + (nch > 1 ? align256(size_t(nch) * d->E * sizeof(int)) : 0);
 }
+// --- tensor-core prefill path (NVFP4) ---------------------------------------
+int ffn_path(const ftmoe_layer_desc* d, int T) {
+  if (d->fmt == FTMOE_NVFP4 && T >= FTMOE_PREFILL_MIN_T && d->d % kStageK == 0 && d->ffn % kStageK == 0) return 1;
+  return 0;
+}
+// N tile of the gate/up GEMM: NH gate rows + NH up rows
+int gate_up_nh(const ftmoe_layer_desc* d) { return d->ffn % 96 == 0 ? 96 : 64; }
+
+inline size_t align1k(size_t v) { return (v + 1023) & ~size_t(1023); }
+
+// Padded row capacity: every resident expert's rows rounded up to 128.
+size_t tc_rows_cap(const ftmoe_layer_desc* d, int T) {
+  const size_t P = size_t(T) * d->k;
+  const size_t r = P + size_t(kTileM - 1) * std::min<size_t>(d->E, P);
+  return (r + kTileM - 1) / kTileM * kTileM;
+}
+
+// header | xq [R][d/2] | sfa [R][d/16] | hq [R][f/2] | sfh [R][f/16]
+struct TcWs {
+  size_t rows, xq, sfa, hq, sfh, total;
+};
+TcWs tc_ws(const ftmoe_layer_desc* d, int T) {
+  TcWs w;
+  w.rows = tc_rows_cap(d, T);
+  size_t o = align1k(kWsHeader);
+  w.xq = o; o += align1k(w.rows * d->d / 2);
+  w.sfa = o; o += align1k(w.rows * d->d / 16);
+  w.hq = o; o += align1k(w.rows * d->ffn / 2);
+  w.sfh = o; o += align1k(w.rows * d->ffn / 16);
+  w.total = o;
+  return w;
+}
+
 size_t ffn_ws(const ftmoe_layer_desc* d, int T) {
+  if (ffn_path(d, T) == 1) return tc_ws(d, T).total;
   const size_t P = size_t(T) * d->k;
   return kWsHeader + align256(P * d->ffn * sizeof(float));
+}
+
+// prepared scale blocks: gate/up [C][f/NH][d/64][atoms][512] | down [C][d/128][f/64][512]
+size_t prep_gate_up_bytes(const ftmoe_layer_desc* d, int C) {
+  const int nh = gate_up_nh(d);
+  return size_t(C) * (d->ffn / nh) * (d->d / 64) * ((2 * nh + 127) / 128) * kSfBlock;
+}
+size_t prep_down_bytes(const ftmoe_layer_desc* d, int C) {
+  return size_t(C) * (d->d / 128) * (d->ffn / 64) * kSfBlock;
+}
+size_t prep_bytes(const ftmoe_layer_desc* d, int C) {
+  if (d->fmt != FTMOE_NVFP4 || d->d % kStageK || d->ffn % kStageK) return 0;
+  return align1k(prep_gate_up_bytes(d, C)) + prep_down_bytes(d, C);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D byte matrix [rows][row_bytes], boxes of 128 bytes x box_rows, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, size_t row_bytes, size_t rows, int box_rows) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cuuint64_t(row_bytes), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
+  cuuint32_t box[2] = {128u, cuuint32_t(box_rows)};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 ftmoe_status route_impl(const ftmoe_layer_desc* d, const uint16_t* x, const uint16_t* wr, const float* bias, int T,
@@ -170,6 +248,89 @@ bool weights_ok(const ftmoe_layer_desc* d, const ftmoe_weights* w) {
   return true;
 }
 
+template <int MODE, int NH>
+ftmoe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb0, const CUtensorMap& tb1, const GemmArgs& g,
+                         int max_tiles, cudaStream_t st) {
+  const int grid = std::max(1, std::min(num_sms(), max_tiles));
+  return launch(gemm_kernel<MODE, NH>, dim3(grid), dim3(kGemmThreads), size_t(GemmCfg<MODE, NH>::SMEM), st, ta, tb0,
+                tb1, g);
+}
+
+// Path 1: gather + quantise x, gate/up GEMM (SwiGLU + quantise h), down GEMM (fused combine or y).
+// zero_out: optional fp32 [T][d] zeroed by the first kernel (the layer call's accumulator).
+ftmoe_status ffn_tc_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of,
+                         const uint16_t* x, int T, const int32_t* off, const int32_t* sp, const float* topk_w,
+                         float* y_or_out, void* ws, float* zero_out, cudaStream_t st) {
+  if (!w->prepared || !aligned16(w->prepared)) return FTMOE_ERR_INVALID_ARG;
+  const TcWs L = tc_ws(d, T);
+  char* base = static_cast<char*>(ws);
+  uint8_t* xq = reinterpret_cast<uint8_t*>(base + L.xq);
+  uint8_t* sfa = reinterpret_cast<uint8_t*>(base + L.sfa);
+  uint8_t* hq = reinterpret_cast<uint8_t*>(base + L.hq);
+  uint8_t* sfh = reinterpret_cast<uint8_t*>(base + L.sfh);
+  const int P = T * d->k;
+  const int nh = gate_up_nh(d);
+  const int sms = num_sms();
+
+  ActqArgs q;
+  q.x = x;
+  q.T = T;
+  q.d = d->d;
+  q.k = d->k;
+  q.E = d->E;
+  q.C = w->C;
+  q.P = P;
+  q.offsets = off;
+  q.sorted_pair = sp;
+  q.slot_of = slot_of;
+  q.xq = xq;
+  q.sfa = sfa;
+  q.rows_cap = int(L.rows);
+  q.zero_out = reinterpret_cast<float4*>(zero_out);
+  q.zero_n4 = zero_out ? (long long)T * d->d / 4 : 0;
+  ftmoe_status s = launch(actq_gather_kernel, dim3(std::min(cdiv(L.rows, kActqWarps), sms * 8)),
+                          dim3(kActqWarps * 32), 0, st, q);
+  if (s != FTMOE_OK) return s;
+
+  CUtensorMap tA1, tG, tU, tA2, tD;
+  const size_t C = size_t(w->C);
+  if (!make_map(&tA1, xq, d->d / 2, L.rows, kTileM) || !make_map(&tG, w->gate, d->d / 2, C * d->ffn, nh) ||
+      !make_map(&tU, w->up, d->d / 2, C * d->ffn, nh) || !make_map(&tA2, hq, d->ffn / 2, L.rows, kTileM) ||
+      !make_map(&tD, w->down, d->ffn / 2, C * d->d, 128))
+    return FTMOE_ERR_CUDA;
+
+  const uint8_t* prep = static_cast<const uint8_t*>(w->prepared);
+  GemmArgs g;
+  g.E = d->E;
+  g.k = d->k;
+  g.d = d->d;
+  g.f = d->ffn;
+  g.C = w->C;
+  g.P = P;
+  g.rows_cap = int(L.rows);
+  g.offsets = off;
+  g.sorted_pair = sp;
+  g.slot_of = slot_of;
+  g.tscale = w->tensor_scale;
+  g.sfa = sfa;
+  g.sfb = prep;
+  g.hq = hq;
+  g.sfh = sfh;
+  g.topk_w = nullptr;
+  g.out = nullptr;
+  const int mts = int(L.rows / kTileM);
+  s = nh == 96 ? launch_gemm<0, 96>(tA1, tG, tU, g, mts * (d->ffn / 96), st)
+               : launch_gemm<0, 64>(tA1, tG, tU, g, mts * (d->ffn / 64), st);
+  if (s != FTMOE_OK) return s;
+  g.sfa = sfh;
+  g.sfb = prep + align1k(prep_gate_up_bytes(d, w->C));
+  g.hq = nullptr;
+  g.sfh = nullptr;
+  g.topk_w = topk_w;
+  g.out = y_or_out;
+  return launch_gemm<1, 128>(tA2, tD, tD, g, mts * (d->d / 128), st);
+}
+
 ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of, const uint16_t* x,
                       int T, const int32_t* off, const int32_t* sp, const float* topk_w, float* y_or_out, void* ws,
                       cudaStream_t st) {
@@ -195,6 +356,7 @@ ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const i
   a.y_or_out = y_or_out;
   a.h = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
   const int P = T * d->k;
+  if (ffn_path(d, T) == 1) return ffn_tc_impl(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, nullptr, st);
   switch (d->fmt) {
     case FTMOE_BF16: return ffn_stream_launch<FTMOE_BF16>(a, P, st);
     case FTMOE_NVFP4: return ffn_stream_launch<FTMOE_NVFP4>(a, P, st);
@@ -291,7 +453,38 @@ size_t ftmoe_expert_ffn_workspace_size(const ftmoe_layer_desc* d, int T) {
 
 int ftmoe_expert_ffn_path(const ftmoe_layer_desc* d, int T) {
   if (!desc_ok(d) || T < 1) return -1;
-  return 0;
+  return ffn_path(d, T);
+}
+
+size_t ftmoe_prepare_weights_size(const ftmoe_layer_desc* d, int C) {
+  if (!desc_ok(d) || C < 1) return 0;
+  return prep_bytes(d, C);
+}
+
+ftmoe_status ftmoe_prepare_weights(const ftmoe_layer_desc* d, const ftmoe_weights* w, void* prep, size_t bytes,
+                                   void* stream) {
+  if (!desc_ok(d) || !weights_ok(d, w)) return FTMOE_ERR_INVALID_ARG;
+  const size_t need = prep_bytes(d, w->C);
+  if (need == 0) return FTMOE_OK;
+  if (!prep || !aligned16(prep)) return FTMOE_ERR_INVALID_ARG;
+  if (bytes < need) return FTMOE_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  uint8_t* out = static_cast<uint8_t*>(prep);
+  const int grid = num_sms() * 4;
+  ftmoe_status s = launch(prep_sf_gate_up_kernel, dim3(grid), dim3(256), 0, st,
+                          static_cast<const uint8_t*>(w->gate_scale), static_cast<const uint8_t*>(w->up_scale), w->C,
+                          d->d, d->ffn, gate_up_nh(d), out);
+  if (s != FTMOE_OK) return s;
+  return launch(prep_sf_down_kernel, dim3(grid), dim3(256), 0, st, static_cast<const uint8_t*>(w->down_scale), w->C,
+                d->d, d->ffn, out + align1k(prep_gate_up_bytes(d, w->C)));
+}
+
+ftmoe_status ftmoe_quantize_act(const ftmoe_layer_desc* d, const uint16_t* x, int T, uint8_t* codes, uint8_t* scales,
+                                void* stream) {
+  if (!desc_ok(d) || T < 1 || T > kMaxT || !x || !codes || !scales) return FTMOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u)) return FTMOE_ERR_INVALID_ARG;
+  return launch(quantize_act_kernel, dim3(std::min(cdiv(T, kActqWarps), num_sms() * 8)), dim3(kActqWarps * 32), 0,
+                as_stream(stream), x, T, d->d, codes, scales);
 }
 
 ftmoe_status ftmoe_expert_ffn(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of,
@@ -405,7 +598,8 @@ LayerWs layer_ws(const ftmoe_layer_desc* d, int T) {
   L.off = o; o += align256(size_t(d->E + 1) * 4);
   L.sp = o; o += align256(P * 4);
   L.pp = o; o += align256(P * 4);
-  L.y = o; o += align256(P * d->d * sizeof(float));
+  L.y = o;
+  if (ffn_path(d, T) == 0) o += align256(P * d->d * sizeof(float));
   L.scratch = o;
   // scratch regions reuse the same bytes after the header, so offset them by the header size
   const size_t sr = route_ws(d, T, true) - kWsHeader;
@@ -466,6 +660,12 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
     }
   }
   if (s != FTMOE_OK) return s;
+  if (ffn_path(d, T) == 1) {
+    // tensor-core path: out_f32 is zeroed by the first FFN kernel and the down GEMM adds w * y into it
+    s = ffn_tc_impl(d, w, slot_of, x, T, off, sp, w_, out_f32, view, out_f32, st);
+    if (s != FTMOE_OK || !out_bf16) return s;
+    return combine_impl(d, T, nullptr, pp, w_, ids_, slot_of, out_f32, out_f32, out_bf16, st);
+  }
   s = ffn_impl(d, w, slot_of, x, T, off, sp, nullptr, y, view, st);
   if (s != FTMOE_OK) return s;
   return combine_impl(d, T, y, pp, w_, ids_, slot_of, nullptr, out_f32, out_bf16, st);

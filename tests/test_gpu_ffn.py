@@ -61,7 +61,9 @@ def test_ffn_and_combine_match_oracle(fmt, E, k, d, f, T):
     slot_np = ((np.arange(E) * 5 + 3) % E).astype(np.int32)
     if E % 5 == 0:
         slot_np = np.arange(E, dtype=np.int32)[::-1].copy()
-    ref = OF.layer(weights_to_numpy(W), slot_np, bf16_bits(x), bf16_bits(wr), bias, k, 1)
+    ft.prepare_weights(dsc, Wd)
+    aq = {0: None, 1: "nvfp4"}[ft.expert_ffn_path(dsc, T)]   # the oracle mirrors the path's quantiser
+    ref = OF.layer(weights_to_numpy(W), slot_np, bf16_bits(x), bf16_bits(wr), bias, k, 1, act_quant=aq)
     xd = x.cuda()
     ids, w, _ = route(dsc, xd, wr.cuda(), None if bias is None else torch.from_numpy(bias).cuda())
     off, sp, pp = permute(dsc, ids)

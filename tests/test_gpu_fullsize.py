@@ -40,7 +40,9 @@ def _weights(w: synth.Workload, seed=0):
         _cache.clear()
         torch.cuda.empty_cache()
         L = w.layer
-        _cache[key] = synth.make_experts(L.fmt, L.E, L.d, L.f, seed, device="cuda")
+        W = synth.make_experts(L.fmt, L.E, L.d, L.f, seed, device="cuda")
+        ft.prepare_weights(ft.desc(L.E, L.k, L.d, L.f, L.fmt), W)
+        _cache[key] = W
     return _cache[key]
 
 
