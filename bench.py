@@ -3,14 +3,15 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
-A step is one pass of the whole hot path over one batch of synthetic input:
+A step is one pass of the whole hot path over one batch of synthetic input,
+through the library's layer call (ftmoe_layer_forward):
   * route (logits, top-k, weights);
   * permute (expert-sorted pairs);
-  * the global-LRU access of the step's experts, on a side stream;
   * the expert FFN;
-  * the weighted combine to bf16.
-The FFN is timed with the step's experts resident.  In the `stack` workloads
-a step runs the batch through all 8 layers.
+  * the weighted combine to bf16;
+plus the global-LRU access of the step's experts (ftmoe_slot_lru) on a side
+stream.  The FFN is timed with the step's experts resident.  In the `stack`
+workloads a step runs the batch through all 8 layers.
 
 Default workload: decode, 128 experts top-8, d 2048, ffn 768, NVFP4, batch 1
 (MoE-layer tokens/s at decode).  Successive steps cycle through 16 distinct
@@ -54,12 +55,14 @@ WORKLOADS = {
     "tiny": (synth.TINY, 16, 64),
 }
 METRIC = "MoE-layer tokens/s"
+DEFAULT_STEPS = {"decode": 40000, "decode4": 30000, "decode16": 20000, "prefill": 1000, "stack1": 4000,
+                 "stack16": 2000, "stack64": 1000, "prefill_split": 200, "tiny": 40000}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (default: per workload, about a second)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
@@ -198,6 +201,34 @@ def ncu_traffic(workload: str):
     return ent.get("bytes_per_call")
 
 
+def new_graph():
+    try:
+        return torch.cuda.CUDAGraph(keep_graph=True)
+    except TypeError:
+        return torch.cuda.CUDAGraph()
+
+
+def graph_kernel_nodes(graph):
+    """Kernel nodes of a captured graph (every one is a launch of this library), or None."""
+    try:
+        from cuda.bindings import runtime as rt
+        g = graph.raw_cuda_graph()
+        err, _, n = rt.cudaGraphGetNodes(g, 0)
+        if int(err) != 0:
+            return None
+        err, nodes, n = rt.cudaGraphGetNodes(g, n)
+        if int(err) != 0:
+            return None
+        kern = 0
+        for nd in nodes:
+            err, typ = rt.cudaGraphNodeGetType(nd)
+            if int(err) == 0 and int(typ) == int(rt.cudaGraphNodeType.cudaGraphNodeTypeKernel):
+                kern += 1
+        return kern
+    except Exception:
+        return None
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -215,11 +246,13 @@ def bench_ours(args, rank, ws):
     n_x = 64
     xs = [synth.make_x(T, L.d, 77 + 1000 * rank + i, device=dev) for i in range(n_x)]
     P = T * L.k
-    ids = torch.empty(T, L.k, dtype=torch.int32, device=dev)
-    tw = torch.empty(T, L.k, dtype=torch.float32, device=dev)
+    nl_step = n_layers if stack else 1
+    # ids / weights per (buffer b, layer in the step): the side stream's LRU reads step i's ids
+    # while step i + 1 runs, so steps alternate between two buffers
+    ids = [[torch.empty(T, L.k, dtype=torch.int32, device=dev) for _ in range(nl_step)] for _ in range(2)]
+    tw = [[torch.empty(T, L.k, dtype=torch.float32, device=dev) for _ in range(nl_step)] for _ in range(2)]
     off = torch.empty(L.E + 1, dtype=torch.int32, device=dev)
     sp = torch.empty(P, dtype=torch.int32, device=dev)
-    pp = torch.empty(P, dtype=torch.int32, device=dev)
     y = torch.empty(P, L.d, dtype=torch.float32, device=dev)
     out = torch.empty(T, L.d, dtype=torch.float32, device=dev)
     out_bf = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
@@ -228,9 +261,8 @@ def bench_ours(args, rank, ws):
     ws_f = ft.workspace(ft.expert_ffn_workspace_size(dsc, T))
     ws_l = ft.workspace(ft.layer_workspace_size(dsc, T))
     path = ft.expert_ffn_path(dsc, T)
-    if path == 1:   # the tensor-core path reads repacked block scales (prepared once, outside timing)
-        for l in layers:
-            ft.prepare_weights(dsc, l.W)
+    for l in layers:   # derived layouts the fast kernels read (prepared once, outside timing)
+        ft.prepare_weights(dsc, l.W)
     structs = [ft.weights_struct(l.W) for l in layers]
     lru = ft.LRU(wl.layers if stack else 1, L.E, wl.capacity or L.E)
     cap = min(P, L.E)
@@ -240,42 +272,59 @@ def bench_ours(args, rank, ws):
     lcnt = torch.zeros(2, dtype=torch.int64, device=dev)
     main = torch.cuda.Stream()
     side = torch.cuda.Stream()
-    ev_fork = [torch.cuda.Event() for _ in range(2)]
+    ev_main = [[torch.cuda.Event() for _ in range(nl_step)] for _ in range(2)]
+    ev_side = [[torch.cuda.Event() for _ in range(nl_step)] for _ in range(2)]
 
-    def one_layer(li, x, lru_layer):
+    recorded = set()     # (b, j) whose side event was recorded in the current capture / warm-up
+
+    def one_layer(li, x, j, b):
+        """Layer li through ftmoe_layer_forward (route, permute, expert FFN, combine) on the main
+        stream; the global-LRU access of its experts on the side stream."""
         l = layers[li]
-        ft.route(dsc, x, l.wr, l.bias, ids, tw, None, ws_r, main)
-        ft.permute(dsc, ids, off, sp, pp, ws_p, main)
-        # the LRU decision runs beside the FFN on a side stream
-        ev_fork[0].record(main)
-        side.wait_event(ev_fork[0])
-        lru.step(lru_layer, ids, hit, lslot, lev, lcnt, side)
-        ev_fork[1].record(side)
-        ft.expert_ffn(dsc, structs[li], None, x, off, sp, None, y, ws_f, main)
-        ft.combine(dsc, T, y, pp, tw, ids, None, None, out, out_bf, main)
-        main.wait_event(ev_fork[1])
+        if (b, j) in recorded:
+            main.wait_event(ev_side[b][j])   # the LRU of two steps ago has read ids[b][j]
+        ft.layer_forward(dsc, structs[li], None, x, l.wr, l.bias, ids[b][j], tw[b][j], out, out_bf, ws_l, main)
+        ev_main[b][j].record(main)
+        side.wait_event(ev_main[b][j])
+        lru.step(j if stack else 0, ids[b][j], hit, lslot, lev, lcnt, side)
+        ev_side[b][j].record(side)
+        recorded.add((b, j))
 
     def step(i):
         x = xs[i % n_x]
+        b = i % 2
         if stack:
             for li in range(n_layers):
-                one_layer(li, x, li)
+                one_layer(li, x, li, b)
         else:
-            one_layer(i % n_layers, x, 0)
+            one_layer(i % n_layers, x, 0, b)
+
+    def join_side():
+        for b, j in sorted(recorded):
+            main.wait_event(ev_side[b][j])
+        recorded.clear()
 
     # eager warm-up (also loads every kernel), then capture K steps into one graph
     with torch.cuda.stream(main):
         for i in range(max(1, args.warmup)):
             step(i)
+        join_side()
     torch.cuda.synchronize()
 
     K = args.steps
-    graph = torch.cuda.CUDAGraph()
+    # one graph of G steps, replayed K / G times inside the timed region (G divides K)
+    G = min(K, 1000)
+    while K % G:
+        G -= 1
+    graph = new_graph()
     with torch.cuda.graph(graph, stream=main):
-        for i in range(K):
+        for i in range(G):
             step(i)
+        join_side()
+    nodes = graph_kernel_nodes(graph)
+    launches_in_graph = None if nodes is None else nodes * (K // G)
     with torch.cuda.stream(main):     # replay() launches on the current stream
-        for _ in range(max(3, args.warmup // max(1, K) + 1)):
+        for _ in range(max(3, args.warmup // max(1, G) + 1)):
             graph.replay()
     torch.cuda.synchronize()
 
@@ -288,7 +337,8 @@ def bench_ours(args, rank, ws):
     t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(main):
         t0.record(main)
-        graph.replay()
+        for _ in range(K // G):
+            graph.replay()
         t1.record(main)
     t1.synchronize()
     torch.cuda.synchronize()
@@ -298,13 +348,10 @@ def bench_ours(args, rank, ws):
     ms_max = max_over_ranks(ms, ws)
     tokens = T * K * ws
     value = tokens / (ms_max / 1e3)
-    launches_per_layer = 1 + (1 if T > 64 else 0)  # route
-    n_perm = 1 if P <= 1024 else 2
-    launches_per_layer += n_perm + 1 + (3 if path == 1 else 2) + 1     # permute, lru, ffn, combine
-    gpu_launches = K * launches_per_layer * (n_layers if stack else 1)
+    gpu_launches = launches_in_graph
 
     # --- dominant call (expert FFN) timed alone over the same steps ----------
-    n_ffn = min(K, 256)
+    n_ffn = min(G, 256)
     sev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ffn)]
     eev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ffn)]
     uniq = []
@@ -315,21 +362,22 @@ def bench_ours(args, rank, ws):
             li = i % n_layers
             x = xs[i % n_x]
             l = layers[li]
-            r_ids = torch.empty_like(ids)
-            r_w = torch.empty_like(tw)
+            r_ids = torch.empty(T, L.k, dtype=torch.int32, device=dev)
+            r_w = torch.empty(T, L.k, dtype=torch.float32, device=dev)
             r_off = torch.empty_like(off)
             r_sp = torch.empty_like(sp)
-            r_pp = torch.empty_like(pp)
+            r_pp = torch.empty_like(sp)
             ft.route(dsc, x, l.wr, l.bias, r_ids, r_w, None, ws_r, main)
             ft.permute(dsc, r_ids, r_off, r_sp, r_pp, ws_p, main)
-            routes.append((li, x, r_ids, r_off, r_sp))
+            routes.append((li, x, r_ids, r_off, r_sp, r_w))
     torch.cuda.synchronize()
-    for li, x, r_ids, r_off, r_sp in routes:
+    for li, x, r_ids, r_off, r_sp, r_w in routes:
         uniq.append(len(np.unique(r_ids.cpu().numpy())))
+    out.zero_()
     with torch.cuda.graph(g2, stream=main):
-        for i, (li, x, r_ids, r_off, r_sp) in enumerate(routes):
+        for i, (li, x, r_ids, r_off, r_sp, r_w) in enumerate(routes):
             sev[i].record(main)
-            ft.expert_ffn(dsc, structs[li], None, x, r_off, r_sp, None, y, ws_f, main)
+            ft.expert_ffn(dsc, structs[li], None, x, r_off, r_sp, r_w, out, ws_f, main)
             eev[i].record(main)
     with torch.cuda.stream(main):
         g2.replay()
@@ -466,7 +514,7 @@ def blas_threads() -> int:
 
 def bench_reference(args, rank, ws):
     wl, T, n_layers = WORKLOADS[args.workload]
-    budget = min(150.0, max(10.0, 0.05 * args.steps))
+    budget = 20.0     # seconds of oracle work: a bounded sample of the workload
     for _ in range(max(0, min(args.warmup, 1))):
         oracle_rate(args.workload, 0.0, max_steps=1)
     rate, threads, sample, el = oracle_rate(args.workload, budget, max_steps=args.steps)
@@ -484,6 +532,8 @@ def bench_reference(args, rank, ws):
 
 def main():
     args = parse()
+    if args.steps <= 0:
+        args.steps = DEFAULT_STEPS[args.workload]
     if args.impl == "reference":
         # the oracle runs on the host cores of rank 0 only; other ranks exit without work
         if int(os.environ.get("RANK", "0")) == 0:

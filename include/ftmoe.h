@@ -99,27 +99,39 @@ typedef struct {
   const void* up_scale;
   const void* down_scale;
   const float* tensor_scale;
-  /* Scales repacked by ftmoe_prepare_weights for the tensor-core path, or NULL.
-   * Required when ftmoe_expert_ffn_path reports 1 for the call (NVFP4 prefill);
-   * the streaming path ignores it. */
+  /* Layouts derived by ftmoe_prepare_weights, or NULL.  Required when
+   * ftmoe_expert_ffn_path reports 1 for the call (NVFP4 prefill); the decode
+   * path of NVFP4 / MXFP4 runs faster with it. */
   const void* prepared;
 } ftmoe_weights;
 
 /* ---------------------------------------------------------------------------
- * ftmoe_prepare_weights - repack the NVFP4 block scales of a slot arena for the
- * tensor-core path.  Run once per arena (or after slots are refilled), outside
- * any timed region; the codes themselves are used in place.
- * Each MMA with K = 64 reads four scales per row from tensor memory.  The
- * repacked layout holds, per 128 weight rows and per K = 64 step, the 512 bytes
- * that one tcgen05.cp moves there: byte (r % 32) * 16 + (r / 32) * 4 + kb for
- * row r of the 128 and 16-element block kb of the 64.
- *   gate/up  [C][ffn/NH][d/64][A][512]: an N tile of NH gate rows then NH up rows
- *            (NH = 96 if ffn % 96 == 0, else 64) in A = ceil(2*NH/128) blocks of
- *            128 rows, zero past 2*NH rows
- *   down     [C][d/128][ffn/64][512]
+ * ftmoe_prepare_weights - derived layouts of a slot arena that the fast kernels
+ * read.  Run once per arena (or after slots are refilled), outside any timed
+ * region.  The canonical arena stays the interchange format.  Two parts, in this
+ * order in prep:
+ *   1. Prefill (NVFP4, d and ffn multiples of 256): the weight block scales
+ *      repacked for the tensor-core path.  Each MMA with K = 64 reads four scales
+ *      per row from tensor memory; per 128 weight rows and per K = 64 step the
+ *      layout holds the 512 bytes that one tcgen05.cp moves there: byte
+ *      (r % 32) * 16 + (r / 32) * 4 + kb for row r of the 128 and 16-element
+ *      block kb of the 64.  The tensor-core path reads the codes in place.
+ *        gate/up  [C][ffn/NH][d/64][A][512]: an N tile of NH gate rows then NH up
+ *                 rows (NH = 96 if ffn % 96 == 0, else 64) in A = ceil(2*NH/128)
+ *                 blocks of 128 rows, zero past 2*NH rows
+ *        down     [C][d/128][ffn/64][512]
+ *   2. Decode (NVFP4, MXFP4), starting at the next 1024-byte boundary: a copy of
+ *      codes and scales in tiles that each stream into shared memory with one
+ *      bulk copy, ordered so that warp-level MMA fragments read them without bank
+ *      conflicts.  Per slot: ffn/16 gate/up tiles then d/32 down tiles.  A tile of
+ *      R rows of one matrix holds its codes as [K/32][R][16 bytes] and its scales
+ *      as [K/16 or K/32][R]; a gate/up tile is [gate codes][up codes][gate
+ *      scales][up scales] (R = 16), a down tile [codes][scales] (R = 32).  Its
+ *      size equals the canonical bytes of the slot.  Without it (weights->prepared
+ *      NULL) the decode path reads the canonical arena, more slowly.
  * weights->prepared is ignored here.  prep (device, prep_bytes from
  * ftmoe_prepare_weights_size, 256-byte aligned) is written; it is then passed as
- * weights->prepared.  Formats other than NVFP4 need nothing: size 0, and the call
+ * weights->prepared.  BF16 and FP8_B128 need nothing: size 0, and the call
  * returns FTMOE_OK without work.
  * ------------------------------------------------------------------------- */
 size_t ftmoe_prepare_weights_size(const ftmoe_layer_desc* desc, int C);

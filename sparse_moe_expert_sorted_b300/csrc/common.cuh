@@ -21,6 +21,11 @@ enum DevErr : int {
   DEV_ERR_LRU_CAPACITY = 3,  // replay output buffer too small
   DEV_ERR_BAD_LAYER = 4,
   DEV_ERR_LRU_STATE = 5,     // the recency list is inconsistent (never expected)
+  DEV_ERR_TIMEOUT = 6,       // a bounded wait on an mbarrier gave up
+  DEV_ERR_BAD_PAIR = 7,      // a sorted pair index outside [0, P)
+  DEV_ERR_ROWS = 8,          // padded rows beyond the workspace's capacity
+  DEV_ERR_NONFINITE = 9,     // a non-finite FFN value (inputs beyond the f16 range on the decode path)
+  DEV_ERR_GRID_TIMEOUT = 10, // a bounded grid barrier gave up
 };
 
 __device__ __forceinline__ void set_dev_err(int code) { atomicCAS(&g_dev_err, 0, code); }
@@ -37,6 +42,8 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // are zero between calls; buffers follow at 256-byte aligned offsets.
 constexpr size_t kWsCounterRoute = 0;     // uint32
 constexpr size_t kWsCounterPermute = 4;   // uint32
+constexpr size_t kWsBarrierCount = 16;    // uint32: grid barrier arrivals (back to 0 after each barrier)
+constexpr size_t kWsBarrierGen = 20;      // uint32: grid barrier generation (only ever incremented)
 constexpr size_t kWsHeader = FTMOE_WS_ZERO_BYTES;
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 

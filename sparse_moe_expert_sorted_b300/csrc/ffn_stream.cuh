@@ -46,6 +46,10 @@ struct FfnArgs {
   const float* topk_w;     // nullptr: write y; else add w*y into out
   float* y_or_out;
   float* h;                // [P][f]
+  // layer call only (decode kernel): zero y_or_out (the fused-combine accumulator) before any
+  // add, and afterwards write its bf16 copy here (nullptr = neither)
+  uint16_t* out_bf16;
+  const uint8_t* prep_dec;  // prepared decode layout of the arena (NVFP4 / MXFP4), or nullptr
 };
 
 template <int FMT>

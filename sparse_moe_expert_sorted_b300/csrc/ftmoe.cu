@@ -7,6 +7,8 @@
 
 #include "common.cuh"
 #include "combine.cuh"
+#include "decode.cuh"
+#include "decode_stream.cuh"
 #include "ffn_stream.cuh"
 #include "lru.cuh"
 #include "permute.cuh"
@@ -108,14 +110,16 @@ size_t tc_rows_cap(const ftmoe_layer_desc* d, int T) {
   return (r + kTileM - 1) / kTileM * kTileM;
 }
 
-// header | xq [R][d/2] | sfa [R][d/16] | hq [R][f/2] | sfh [R][f/16]
+// header | xq_tok [T][d/2] | sf_tok [T][d/16] | xq [R][d/2] | sfa [R][d/16] | hq [R][f/2] | sfh [R][f/16]
 struct TcWs {
-  size_t rows, xq, sfa, hq, sfh, total;
+  size_t rows, xq_tok, sf_tok, xq, sfa, hq, sfh, total;
 };
 TcWs tc_ws(const ftmoe_layer_desc* d, int T) {
   TcWs w;
   w.rows = tc_rows_cap(d, T);
   size_t o = align1k(kWsHeader);
+  w.xq_tok = o; o += align1k(size_t(T) * d->d / 2);
+  w.sf_tok = o; o += align1k(size_t(T) * d->d / 16);
   w.xq = o; o += align1k(w.rows * d->d / 2);
   w.sfa = o; o += align1k(w.rows * d->d / 16);
   w.hq = o; o += align1k(w.rows * d->ffn / 2);
@@ -138,9 +142,19 @@ size_t prep_gate_up_bytes(const ftmoe_layer_desc* d, int C) {
 size_t prep_down_bytes(const ftmoe_layer_desc* d, int C) {
   return size_t(C) * (d->d / 128) * (d->ffn / 64) * kSfBlock;
 }
-size_t prep_bytes(const ftmoe_layer_desc* d, int C) {
+// prepared buffer: [prefill scale blocks (NVFP4, d and ffn multiples of 256)][decode layout (NVFP4, MXFP4)]
+size_t prep_prefill_bytes(const ftmoe_layer_desc* d, int C) {
   if (d->fmt != FTMOE_NVFP4 || d->d % kStageK || d->ffn % kStageK) return 0;
   return align1k(prep_gate_up_bytes(d, C)) + prep_down_bytes(d, C);
+}
+size_t prep_decode_offset(const ftmoe_layer_desc* d, int C) { return align1k(prep_prefill_bytes(d, C)); }
+size_t prep_decode_bytes(const ftmoe_layer_desc* d, int C) {
+  if (d->fmt != FTMOE_NVFP4 && d->fmt != FTMOE_MXFP4) return 0;
+  return size_t(C) * sd_slot_bytes(d->d, d->ffn, d->fmt);
+}
+size_t prep_bytes(const ftmoe_layer_desc* d, int C) {
+  const size_t dec = prep_decode_bytes(d, C);
+  return dec ? prep_decode_offset(d, C) + dec : prep_prefill_bytes(d, C);
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -173,9 +187,20 @@ bool make_map(CUtensorMap* m, const void* base, size_t row_bytes, size_t rows, i
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// perm_*: optional fused permutation (only when the router's last CTA selects, and P fits one CTA);
+// *fused_perm tells whether it was done.
+bool route_can_permute(const ftmoe_layer_desc* d, int T) {
+  return T <= kSelectSmallT && T * d->k <= kPermChunk;
+}
 ftmoe_status route_impl(const ftmoe_layer_desc* d, const uint16_t* x, const uint16_t* wr, const float* bias, int T,
-                        int32_t* ids, float* w, float* logits, void* ws, cudaStream_t st) {
+                        int32_t* ids, float* w, float* logits, void* ws, cudaStream_t st, int32_t* perm_off = nullptr,
+                        int32_t* perm_sp = nullptr, int32_t* perm_pp = nullptr) {
   RouteArgs a;
+  const bool fp = perm_off && route_can_permute(d, T);
+  a.perm_off = fp ? perm_off : nullptr;
+  a.perm_sp = fp ? perm_sp : nullptr;
+  a.perm_pp = fp ? perm_pp : nullptr;
+  const size_t psm = fp ? size_t(permute_block_ints(d->E, kRouteWarps)) * sizeof(int) : 0;
   a.x = x;
   a.wr = wr;
   a.bias = bias;
@@ -194,13 +219,15 @@ ftmoe_status route_impl(const ftmoe_layer_desc* d, const uint16_t* x, const uint
   dim3 blk(kRouteWarps * 32);
   if (T == 1) {
     const int items = d->E;
-    s = launch(route_logits_kernel<1, 1>, dim3(std::min(cdiv(items, kRouteWarps), sms * 8)), blk, 0, st, a, fused);
+    s = launch(route_logits_kernel<1, 1, 8>, dim3(std::min(cdiv(items, kRouteWarps), sms * 8)), blk, psm, st, a,
+               fused);
   } else if (T <= 64) {
     const int items = d->E * cdiv(T, 8);
-    s = launch(route_logits_kernel<1, 8>, dim3(std::min(cdiv(items, kRouteWarps), sms * 8)), blk, 0, st, a, fused);
+    s = launch(route_logits_kernel<1, 8, 2>, dim3(std::min(cdiv(items, kRouteWarps), sms * 8)), blk, psm, st, a,
+               fused);
   } else {
     const long long items = (long long)cdiv(d->E, 4) * cdiv(T, 8);
-    s = launch(route_logits_kernel<4, 8>, dim3((unsigned)std::min<long long>(cdiv(items, kRouteWarps), sms * 8)),
+    s = launch(route_logits_kernel<4, 8, 1>, dim3((unsigned)std::min<long long>(cdiv(items, kRouteWarps), sms * 8)),
                blk, 0, st, a, fused);
   }
   if (s != FTMOE_OK || fused) return s;
@@ -233,6 +260,49 @@ ftmoe_status ffn_stream_launch(const FfnArgs& a, int P, cudaStream_t st) {
                           blk, 0, st, a);
   if (s != FTMOE_OK) return s;
   return launch(ffn_down_kernel<FMT>, dim3((unsigned)std::min<long long>(cdiv(items_d, kFfnWarps), cap)), blk, 0, st, a);
+}
+
+// CTAs of `kern` that fit on one SM with `smem` dynamic bytes (0 on error).
+template <typename K>
+int resident_ctas(K kern, int threads, size_t smem) {
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+// Decode path of the 4-bit block-scaled formats: one persistent kernel whose CTAs are all
+// resident (its two phases meet at a grid barrier), over 16-row units.
+// hdr: the workspace's zero header (grid barrier words).
+int max_smem_optin() {
+  int dev = 0, v = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || v <= 0) v = 232448;
+  return v;
+}
+
+template <int FMT>
+ftmoe_status ffn_dec_launch(const FfnArgs& a, int P, void* hdr, cudaStream_t st) {
+  unsigned* cnt = reinterpret_cast<unsigned*>(static_cast<char*>(hdr) + kWsBarrierCount);
+  unsigned* gen = reinterpret_cast<unsigned*>(static_cast<char*>(hdr) + kWsBarrierGen);
+  const int ms = max_smem_optin();
+  const int xrows = std::min(8, a.T);
+  if (a.prep_dec && sd_supported(a.E, a.d, a.f, FMT, xrows, ms)) {
+    // streaming form: one CTA per SM, bulk copies into a shared-memory ring
+    const SdLayout Ls = sd_layout(a.E, a.d, a.f, FMT, xrows, ms);
+    const int per_sm = resident_ctas(sd_ffn_kernel<FMT>, kSdThreads, size_t(Ls.smem));
+    if (per_sm < 1) return FTMOE_ERR_CUDA;
+    return launch(sd_ffn_kernel<FMT>, dim3(num_sms()), dim3(kSdThreads), size_t(Ls.smem), st, a, Ls, cnt, gen);
+  }
+  const size_t smem = dec_smem_bytes(std::max(a.d, a.f));
+  const int per_sm = resident_ctas(dec_ffn_kernel<FMT>, kDecWarps * 32, smem);
+  if (per_sm < 1) return FTMOE_ERR_CUDA;
+  const long long experts = std::min(a.E, P);
+  const long long units = experts * (std::max(a.d, a.f) / 16);
+  const int grid = (int)std::min<long long>(units, (long long)per_sm * num_sms());
+  return launch(dec_ffn_kernel<FMT>, dim3(grid), dim3(kDecWarps * 32), smem, st, a, cnt, gen);
 }
 
 bool weights_ok(const ftmoe_layer_desc* d, const ftmoe_weights* w) {
@@ -272,8 +342,14 @@ ftmoe_status ffn_tc_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, cons
   const int nh = gate_up_nh(d);
   const int sms = num_sms();
 
+  uint8_t* xq_tok = reinterpret_cast<uint8_t*>(base + L.xq_tok);
+  uint8_t* sf_tok = reinterpret_cast<uint8_t*>(base + L.sf_tok);
+  ftmoe_status s = launch(quantize_act_kernel, dim3(std::min(cdiv(T, kActqWarps), sms * 8)), dim3(kActqWarps * 32), 0,
+                          st, x, T, d->d, xq_tok, sf_tok);
+  if (s != FTMOE_OK) return s;
   ActqArgs q;
-  q.x = x;
+  q.xq_tok = xq_tok;
+  q.sf_tok = sf_tok;
   q.T = T;
   q.d = d->d;
   q.k = d->k;
@@ -288,7 +364,7 @@ ftmoe_status ffn_tc_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, cons
   q.rows_cap = int(L.rows);
   q.zero_out = reinterpret_cast<float4*>(zero_out);
   q.zero_n4 = zero_out ? (long long)T * d->d / 4 : 0;
-  ftmoe_status s = launch(actq_gather_kernel, dim3(std::min(cdiv(L.rows, kActqWarps), sms * 8)),
+  s = launch(actq_gather_kernel, dim3(std::min(cdiv(L.rows, kActqWarps), sms * 8)),
                           dim3(kActqWarps * 32), 0, st, q);
   if (s != FTMOE_OK) return s;
 
@@ -331,9 +407,14 @@ ftmoe_status ffn_tc_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, cons
   return launch_gemm<1, 128>(tA2, tD, tD, g, mts * (d->d / 128), st);
 }
 
+// ws: buffers at ws + kWsHeader; hdr: the zero header that holds the call's counters.
+// out_bf16 (decode kernel only, with topk_w): zero y_or_out first and write its bf16 copy last.
+bool ffn_dec_kernel(const ftmoe_layer_desc* d, int T) {
+  return ffn_path(d, T) == 0 && (d->fmt == FTMOE_NVFP4 || d->fmt == FTMOE_MXFP4);
+}
 ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of, const uint16_t* x,
                       int T, const int32_t* off, const int32_t* sp, const float* topk_w, float* y_or_out, void* ws,
-                      cudaStream_t st) {
+                      void* hdr, cudaStream_t st, uint16_t* out_bf16 = nullptr) {
   FfnArgs a;
   a.E = d->E;
   a.k = d->k;
@@ -355,12 +436,16 @@ ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const i
   a.topk_w = topk_w;
   a.y_or_out = y_or_out;
   a.h = reinterpret_cast<float*>(static_cast<char*>(ws) + kWsHeader);
+  a.out_bf16 = out_bf16;
+  a.prep_dec = (w->prepared && prep_decode_bytes(d, w->C))
+                   ? static_cast<const uint8_t*>(w->prepared) + prep_decode_offset(d, w->C)
+                   : nullptr;
   const int P = T * d->k;
   if (ffn_path(d, T) == 1) return ffn_tc_impl(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, nullptr, st);
   switch (d->fmt) {
     case FTMOE_BF16: return ffn_stream_launch<FTMOE_BF16>(a, P, st);
-    case FTMOE_NVFP4: return ffn_stream_launch<FTMOE_NVFP4>(a, P, st);
-    case FTMOE_MXFP4: return ffn_stream_launch<FTMOE_MXFP4>(a, P, st);
+    case FTMOE_NVFP4: return ffn_dec_launch<FTMOE_NVFP4>(a, P, hdr, st);
+    case FTMOE_MXFP4: return ffn_dec_launch<FTMOE_MXFP4>(a, P, hdr, st);
     case FTMOE_FP8_B128: return ffn_stream_launch<FTMOE_FP8_B128>(a, P, st);
   }
   return FTMOE_ERR_UNSUPPORTED;
@@ -471,12 +556,23 @@ ftmoe_status ftmoe_prepare_weights(const ftmoe_layer_desc* d, const ftmoe_weight
   cudaStream_t st = as_stream(stream);
   uint8_t* out = static_cast<uint8_t*>(prep);
   const int grid = num_sms() * 4;
-  ftmoe_status s = launch(prep_sf_gate_up_kernel, dim3(grid), dim3(256), 0, st,
-                          static_cast<const uint8_t*>(w->gate_scale), static_cast<const uint8_t*>(w->up_scale), w->C,
-                          d->d, d->ffn, gate_up_nh(d), out);
-  if (s != FTMOE_OK) return s;
-  return launch(prep_sf_down_kernel, dim3(grid), dim3(256), 0, st, static_cast<const uint8_t*>(w->down_scale), w->C,
-                d->d, d->ffn, out + align1k(prep_gate_up_bytes(d, w->C)));
+  ftmoe_status s = FTMOE_OK;
+  if (prep_prefill_bytes(d, w->C)) {
+    s = launch(prep_sf_gate_up_kernel, dim3(grid), dim3(256), 0, st, static_cast<const uint8_t*>(w->gate_scale),
+               static_cast<const uint8_t*>(w->up_scale), w->C, d->d, d->ffn, gate_up_nh(d), out);
+    if (s != FTMOE_OK) return s;
+    s = launch(prep_sf_down_kernel, dim3(grid), dim3(256), 0, st, static_cast<const uint8_t*>(w->down_scale), w->C,
+               d->d, d->ffn, out + align1k(prep_gate_up_bytes(d, w->C)));
+    if (s != FTMOE_OK) return s;
+  }
+  if (prep_decode_bytes(d, w->C)) {
+    const uint8_t* g8 = static_cast<const uint8_t*>(w->gate);
+    s = launch(prep_decode_kernel, dim3(grid), dim3(256), 0, st, g8, static_cast<const uint8_t*>(w->up),
+               static_cast<const uint8_t*>(w->down), static_cast<const uint8_t*>(w->gate_scale),
+               static_cast<const uint8_t*>(w->up_scale), static_cast<const uint8_t*>(w->down_scale), w->C, d->d,
+               d->ffn, d->fmt, out + prep_decode_offset(d, w->C));
+  }
+  return s;
 }
 
 ftmoe_status ftmoe_quantize_act(const ftmoe_layer_desc* d, const uint16_t* x, int T, uint8_t* codes, uint8_t* scales,
@@ -493,7 +589,7 @@ ftmoe_status ftmoe_expert_ffn(const ftmoe_layer_desc* d, const ftmoe_weights* w,
   if (!desc_ok(d) || T < 1 || T > kMaxT || !x || !off || !sp || !y_or_out || !ws) return FTMOE_ERR_INVALID_ARG;
   if (!weights_ok(d, w) || !aligned16(x) || !aligned16(y_or_out)) return FTMOE_ERR_INVALID_ARG;
   if (ws_bytes < ffn_ws(d, T)) return FTMOE_ERR_WORKSPACE;
-  return ffn_impl(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, as_stream(stream));
+  return ffn_impl(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, ws, as_stream(stream));
 }
 
 ftmoe_status ftmoe_combine(const ftmoe_layer_desc* d, int T, const float* y, const int32_t* pp, const float* w,
@@ -641,10 +737,10 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
   char* view = base + L.scratch - kWsHeader;
   ftmoe_status s;
   // route: logits go to the scratch region (the view's buffer area)
-  s = route_impl(d, x, wr, bias, T, ids_, w_, reinterpret_cast<float*>(base + L.scratch), base, st);
+  s = route_impl(d, x, wr, bias, T, ids_, w_, reinterpret_cast<float*>(base + L.scratch), base, st, off, sp, pp);
   if (s != FTMOE_OK) return s;
-  // permute: its histogram lives in the scratch region too
-  {
+  // permute: fused into the router for small batches; else its histogram lives in the scratch region too
+  if (!route_can_permute(d, T)) {
     const int P = T * d->k;
     const int nch = cdiv(P, kPermChunk);
     if (nch == 1) {
@@ -666,7 +762,11 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
     if (s != FTMOE_OK || !out_bf16) return s;
     return combine_impl(d, T, nullptr, pp, w_, ids_, slot_of, out_f32, out_f32, out_bf16, st);
   }
-  s = ffn_impl(d, w, slot_of, x, T, off, sp, nullptr, y, view, st);
+  if (ffn_dec_kernel(d, T) && out_bf16) {
+    // decode kernel: fused combine into out_f32, which it zeroes first and casts to bf16 last
+    return ffn_impl(d, w, slot_of, x, T, off, sp, w_, out_f32, view, base, st, out_bf16);
+  }
+  s = ffn_impl(d, w, slot_of, x, T, off, sp, nullptr, y, view, base, st);
   if (s != FTMOE_OK) return s;
   return combine_impl(d, T, y, pp, w_, ids_, slot_of, nullptr, out_f32, out_bf16, st);
 }

@@ -152,4 +152,57 @@ permute_rank_kernel(const int32_t* ids, int P, int E, const int32_t* hist, int n
 
 static inline size_t permute_rank_smem(int E) { return size_t(34) * E * sizeof(int); }
 
+// The same stable counting sort done by one CTA over all P pairs, chunk by chunk in pair
+// order (used by the router's last CTA for small batches).  Shared memory: permute_block_ints(E, nw)
+// ints, nw = warps of the CTA; E <= 4 * blockDim.
+__host__ __device__ inline int permute_block_ints(int E, int nw) { return (nw + 2) * E + 33; }
+
+__device__ void permute_block(const int32_t* ids, int P, int E, int32_t* offsets, int32_t* sorted_pair,
+                              int32_t* pair_pos, int* sm) {
+  const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5;
+  int* s_base = sm;                  // [E]: first position of expert e for the current chunk
+  int* s_wcnt = sm + E;              // [nw][E]: per-warp counts, then per-warp bases
+  int* s_ctot = sm + (nw + 1) * E;   // [E]: the chunk's count per expert
+  int* s_wtot = sm + (nw + 2) * E;   // [33]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_base[e] = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) atomicAdd(&s_base[load_id(ids, p, E)], 1);
+  __syncthreads();
+  const int total = block_exclusive_scan(s_base, E, s_wtot);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) offsets[e] = s_base[e];
+  if (threadIdx.x == 0) offsets[E] = total;
+  for (int base = 0; base < P; base += blockDim.x) {
+    for (int i = threadIdx.x; i < nw * E; i += blockDim.x) s_wcnt[i] = 0;
+    __syncthreads();
+    const int p = base + threadIdx.x;
+    const bool active = p < P;
+    const int e = active ? load_id(ids, p, E) : -1;
+    const uint32_t act = __ballot_sync(0xFFFFFFFFu, active);
+    int rank = 0;
+    if (active) {
+      const uint32_t same = __match_any_sync(act, e);
+      rank = __popc(same & lanemask_lt());
+      if (rank == 0) s_wcnt[warp * E + e] = __popc(same);
+    }
+    __syncthreads();
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+      int run = 0;
+      for (int w = 0; w < nw; ++w) {
+        const int v = s_wcnt[w * E + x];
+        s_wcnt[w * E + x] = run;
+        run += v;
+      }
+      s_ctot[x] = run;
+    }
+    __syncthreads();
+    if (active) {
+      const int pos = s_base[e] + s_wcnt[warp * E + e] + rank;
+      sorted_pair[pos] = p;
+      pair_pos[p] = pos;
+    }
+    __syncthreads();
+    for (int x = threadIdx.x; x < E; x += blockDim.x) s_base[x] += s_ctot[x];
+  }
+}
+
 }  // namespace ftmoe

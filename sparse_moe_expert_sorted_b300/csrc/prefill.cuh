@@ -30,7 +30,8 @@
 // layout once (ftmoe_prepare_weights); activation scales are written in it.
 //
 // Kernels (one stream, in order):
-//   actq_gather_kernel  padded rows of x -> E2M1 codes + scale blocks
+//   quantize_act_kernel x -> per-token E2M1 codes + E4M3 scales (once per token)
+//   actq_gather_kernel  padded rows <- the tokens' codes; scales into scale blocks
 //   gemm_kernel<0, NH>  [gate | up] tile of N = 2 NH columns; epilogue
 //                       h = silu(g) * u, quantised to codes + scale blocks
 //   gemm_kernel<1, 128> down tile of 128 columns; epilogue adds w * y into
@@ -55,9 +56,6 @@ constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = (2 + kEpiWarps) * 32;
 constexpr int kStageK = 256;            // FP4 elements per stage (128 bytes per row)
 constexpr int kSfBlock = 512;           // bytes of one 128-row x K=64 scale block
-constexpr int DEV_ERR_TIMEOUT = 6;
-constexpr int DEV_ERR_BAD_PAIR = 7;
-constexpr int DEV_ERR_ROWS = 8;
 
 // s_mt[e] = first M-tile of expert e (resident experts with rows only); s_mt[E] = total.
 // The total is clamped to max_mt (the workspace's row capacity / 128).
@@ -122,11 +120,31 @@ __device__ __forceinline__ uint32_t quant_nvfp4_16(const float (&v)[16], uint2& 
   return sc;
 }
 
+// The same block quantisation for h inside the GEMM epilogue: one division per
+// block (1 / s), then products.  h codes are not compared bit for bit (h is
+// computed in a different order than the oracle's anyway), so a product that
+// differs from the quotient by an ulp only matters at exact rounding ties.
+__device__ __forceinline__ uint32_t quant_nvfp4_16_fast(const float (&v)[16], uint2& c) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const uint32_t sc = e4m3_code(amax / 6.0f);
+  const float s = e4m3_to_float(uint8_t(sc));
+  const float inv = s > 0.f ? 1.0f / s : 0.f;
+  uint32_t b[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) b[i] = e2m1x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+  c.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+  c.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+  return sc;
+}
+
 // ---------------------------------------------------------------------------
 // a3: gather + quantise the padded rows of x
 // ---------------------------------------------------------------------------
 struct ActqArgs {
-  const uint16_t* x;
+  const uint8_t* xq_tok;   // per-token codes [T][d/2] (quantize_act_kernel)
+  const uint8_t* sf_tok;   // per-token scales [T][d/16]
   int T, d, k, E, C, P;
   const int32_t* offsets;
   const int32_t* sorted_pair;
@@ -166,23 +184,16 @@ __global__ void __launch_bounds__(kActqWarps * 32) actq_gather_kernel(ActqArgs a
       if (p >= 0 && p < a.P) tok = p / a.k;
       else set_dev_err(DEV_ERR_BAD_PAIR);
     }
-    const uint16_t* xr = a.x + size_t(tok < 0 ? 0 : tok) * a.d;
+    const uint8_t* qs = a.xq_tok + size_t(tok < 0 ? 0 : tok) * (a.d / 2);
+    const uint8_t* ss = a.sf_tok + size_t(tok < 0 ? 0 : tok) * nb;
     uint8_t* qr = a.xq + size_t(j) * (a.d / 2);
     for (int base = 0; base < nb; base += 32) {
       const int b = base + lane;
       uint2 c = make_uint2(0u, 0u);
       uint32_t sc = 0;
       if (b < nb && tok >= 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(xr + 16 * b);
-        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        float f[16];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          f[2 * q] = bf16_lo(w[q]);
-          f[2 * q + 1] = bf16_hi(w[q]);
-        }
-        sc = quant_nvfp4_16(f, c);
+        c = __ldg(reinterpret_cast<const uint2*>(qs) + b);
+        sc = __ldg(ss + b);
       }
       if (b < nb) reinterpret_cast<uint2*>(qr)[b] = c;
       // lanes 4g..4g+3 hold the four scale bytes of one K = 64 step: one 32-bit store
@@ -296,7 +307,11 @@ struct GemmCfg {
   static constexpr int OFF_BAR = OFF_SFB + kStages * SFB_BYTES;   // full[S], empty[S], tfull[2], tempty[2], done
   static constexpr int OFF_MISC = OFF_BAR + (2 * kStages + 5) * 8;
   static constexpr int OFF_MT = OFF_MISC + 16;                     // int s_mt[1025], s_tmp[33]
-  static constexpr int SMEM = OFF_MT + (1025 + 33) * 4 + 1024;    // + alignment slack
+  // MODE 1: per epilogue warp, its 32 rows x NH/2 columns of the tile (row stride padded by 4 floats)
+  static constexpr int STG_STRIDE = NH / 2 + 4;
+  static constexpr int OFF_STG = (OFF_MT + (1025 + 33) * 4 + 15) / 16 * 16;
+  static constexpr int STG_BYTES = MODE == 1 ? kEpiWarps * 32 * STG_STRIDE * 4 : 0;
+  static constexpr int SMEM = OFF_STG + STG_BYTES + 1024;        // + alignment slack
   static constexpr uint32_t IDESC = idesc_mxf4(kTileM, N, 0);
   static_assert(N % 16 == 0 && N <= 256, "MMA N");
   static_assert(N + 48 <= 256, "accumulator + scale columns must fit 256 TMEM columns");
@@ -478,15 +493,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           for (int i = 0; i < 16; ++i) {
             const float gg = __uint_as_float(g[b][i]) * tsg;
             const float uu = __uint_as_float(u[b][i]) * tsu;
-            hv[i] = gg / (1.f + expf(-gg)) * uu;
+            hv[i] = __fdividef(gg, 1.f + __expf(-gg)) * uu;
           }
           uint2 c;
-          const uint32_t sc = quant_nvfp4_16(hv, c);
+          const uint32_t sc = quant_nvfp4_16_fast(hv, c);
           const int col = nt * NH + half * (NH / 2) + 16 * b;
           *reinterpret_cast<uint2*>(a.hq + size_t(j) * (a.f / 2) + col / 2) = c;
           a.sfh[sf_offset(j, col / 16, fsteps)] = uint8_t(sc);
         }
-      } else {
+      } else if (!a.topk_w) {
+        // y in sorted order
         constexpr int NB = NH / 32;
         uint32_t v[NB][16];
 #pragma unroll
@@ -497,34 +513,63 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const int lo = a.offsets[e];
         const int i = j - s_mt[e] * kTileM;
         if (i < a.offsets[e + 1] - lo) {
-          const int p = a.sorted_pair[lo + i];
           const float tsd = a.tscale ? a.tscale[slot * 3 + 2] : 1.f;
-          const int col0 = nt * NH + half * (NH / 2);
-          if (a.topk_w) {
-            if (p >= 0 && p < a.P) {
-              const float w = a.topk_w[p] * tsd;
-              float* dst = a.out + size_t(p / a.k) * a.d + col0;
+          float* dst = a.out + size_t(lo + i) * a.d + nt * NH + half * (NH / 2);
 #pragma unroll
-              for (int b = 0; b < NB; ++b)
+          for (int b = 0; b < NB; ++b)
 #pragma unroll
-                for (int i4 = 0; i4 < 4; ++i4)
-                  atomicAdd(reinterpret_cast<float4*>(dst + 16 * b) + i4,
-                            make_float4(w * __uint_as_float(v[b][4 * i4]), w * __uint_as_float(v[b][4 * i4 + 1]),
-                                        w * __uint_as_float(v[b][4 * i4 + 2]), w * __uint_as_float(v[b][4 * i4 + 3])));
-            } else {
-              set_dev_err(DEV_ERR_BAD_PAIR);
-            }
+            for (int i4 = 0; i4 < 4; ++i4)
+              reinterpret_cast<float4*>(dst + 16 * b)[i4] =
+                  make_float4(tsd * __uint_as_float(v[b][4 * i4]), tsd * __uint_as_float(v[b][4 * i4 + 1]),
+                              tsd * __uint_as_float(v[b][4 * i4 + 2]), tsd * __uint_as_float(v[b][4 * i4 + 3]));
+        }
+      }
+      if (MODE == 1 && a.topk_w) {
+        // Fused combine.  Stage w * y of the warp's 32 rows, then add row by row so that
+        // every vector reduction of the warp covers contiguous columns of one or two rows.
+        constexpr int NB = NH / 32;
+        constexpr int HC = NH / 2;                  // columns of this warp
+        float* stg = reinterpret_cast<float*>(smem + Cfg::OFF_STG) + (warp - 2) * 32 * Cfg::STG_STRIDE;
+        const int lo = a.offsets[e];
+        const int i = j - s_mt[e] * kTileM;
+        int tok = -1;
+        float w = 0.f;
+        if (i < a.offsets[e + 1] - lo) {
+          const int p = a.sorted_pair[lo + i];
+          if (p >= 0 && p < a.P) {
+            tok = p / a.k;
+            w = a.topk_w[p] * (a.tscale ? a.tscale[slot * 3 + 2] : 1.f);
           } else {
-            float* dst = a.out + size_t(lo + i) * a.d + col0;
-#pragma unroll
-            for (int b = 0; b < NB; ++b)
-#pragma unroll
-              for (int i4 = 0; i4 < 4; ++i4)
-                reinterpret_cast<float4*>(dst + 16 * b)[i4] =
-                    make_float4(tsd * __uint_as_float(v[b][4 * i4]), tsd * __uint_as_float(v[b][4 * i4 + 1]),
-                                tsd * __uint_as_float(v[b][4 * i4 + 2]), tsd * __uint_as_float(v[b][4 * i4 + 3]));
+            set_dev_err(DEV_ERR_BAD_PAIR);
           }
         }
+        uint32_t v[NB][16];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) tc_ld16(tb + half * HC + 16 * b, v[b]);
+        tc_wait_ld();
+#pragma unroll
+        for (int b = 0; b < NB; ++b) tc_reg_fence(v[b]);
+        float* my = stg + lane * Cfg::STG_STRIDE;
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4)
+            reinterpret_cast<float4*>(my + 16 * b)[i4] =
+                make_float4(w * __uint_as_float(v[b][4 * i4]), w * __uint_as_float(v[b][4 * i4 + 1]),
+                            w * __uint_as_float(v[b][4 * i4 + 2]), w * __uint_as_float(v[b][4 * i4 + 3]));
+        __syncwarp();
+        constexpr int LPR = HC / 4;                 // lanes per row (float4 each)
+        constexpr int RPI = 32 / LPR;               // rows per instruction
+        const int sub = lane / LPR, cl = lane % LPR;
+        const int col0 = nt * NH + half * HC;
+#pragma unroll 4
+        for (int r0 = 0; r0 < 32; r0 += RPI) {
+          const int rr = r0 + sub;
+          const int t_r = __shfl_sync(0xFFFFFFFFu, tok, rr);
+          const float4 val = reinterpret_cast<const float4*>(stg + rr * Cfg::STG_STRIDE)[cl];
+          if (t_r >= 0) atomicAdd(reinterpret_cast<float4*>(a.out + size_t(t_r) * a.d + col0) + cl, val);
+        }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();

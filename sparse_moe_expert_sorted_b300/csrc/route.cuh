@@ -14,6 +14,7 @@
 //   - The bias is added last.
 #pragma once
 #include "common.cuh"
+#include "permute.cuh"
 
 namespace ftmoe {
 
@@ -29,6 +30,10 @@ struct RouteArgs {
   int32_t* ids;
   float* w;
   unsigned* counter;    // zero between calls
+  // optional (layer call, small batches): the last CTA also sorts the pairs (ftmoe_permute's outputs)
+  int32_t* perm_off;
+  int32_t* perm_sp;
+  int32_t* perm_pp;
 };
 
 // Warp-level top-k of one token's E logits.  Lane r ends up holding rank r
@@ -92,7 +97,9 @@ __device__ __forceinline__ void select_token(const RouteArgs& a, int t, int lane
 }
 
 // Each warp: EW experts x TW tokens of logits.  Grid-stride over items.
-template <int EW, int TW>
+// The lane's chunks are loaded RB at a time before any is used, so RB loads per
+// operand are in flight; they are still added in ascending chunk order.
+template <int EW, int TW, int RB>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_logits_kernel(RouteArgs a, int fused_select) {
   pdl_wait();
@@ -111,30 +118,38 @@ route_logits_kernel(RouteArgs a, int fused_select) {
     for (int i = 0; i < EW; ++i)
 #pragma unroll
       for (int j = 0; j < TW; ++j) acc[i][j] = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const int c = s * 32 + lane;
-      uint4 wv[EW], xv[TW];
+    for (int s0 = 0; s0 < S; s0 += RB) {
+      uint4 wv[RB][EW], xv[RB][TW];
 #pragma unroll
-      for (int i = 0; i < EW; ++i) {
-        int e = min(e0 + i, a.E - 1);
-        wv[i] = __ldg(reinterpret_cast<const uint4*>(a.wr + size_t(e) * a.d) + c);
-      }
-#pragma unroll
-      for (int j = 0; j < TW; ++j) {
-        int t = min(t0 + j, a.T - 1);
-        xv[j] = __ldg(reinterpret_cast<const uint4*>(a.x + size_t(t) * a.d) + c);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int b = 0; b < RB; ++b) {
+        const int c = min(s0 + b, S - 1) * 32 + lane;
 #pragma unroll
         for (int i = 0; i < EW; ++i) {
-          const uint32_t ww = (&wv[i].x)[u >> 1];
-          const float wf = (u & 1) ? bf16_hi(ww) : bf16_lo(ww);
+          int e = min(e0 + i, a.E - 1);
+          wv[b][i] = __ldg(reinterpret_cast<const uint4*>(a.wr + size_t(e) * a.d) + c);
+        }
 #pragma unroll
-          for (int j = 0; j < TW; ++j) {
-            const uint32_t xx = (&xv[j].x)[u >> 1];
-            const float xf = (u & 1) ? bf16_hi(xx) : bf16_lo(xx);
-            acc[i][j] = __fadd_rn(acc[i][j], __fmul_rn(xf, wf));
+        for (int j = 0; j < TW; ++j) {
+          int t = min(t0 + j, a.T - 1);
+          xv[b][j] = __ldg(reinterpret_cast<const uint4*>(a.x + size_t(t) * a.d) + c);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < RB; ++b) {
+        if (s0 + b < S) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+#pragma unroll
+            for (int i = 0; i < EW; ++i) {
+              const uint32_t ww = (&wv[b][i].x)[u >> 1];
+              const float wf = (u & 1) ? bf16_hi(ww) : bf16_lo(ww);
+#pragma unroll
+              for (int j = 0; j < TW; ++j) {
+                const uint32_t xx = (&xv[b][j].x)[u >> 1];
+                const float xf = (u & 1) ? bf16_hi(xx) : bf16_lo(xx);
+                acc[i][j] = __fadd_rn(acc[i][j], __fmul_rn(xf, wf));
+              }
+            }
           }
         }
       }
@@ -176,6 +191,11 @@ route_logits_kernel(RouteArgs a, int fused_select) {
   __threadfence();
   for (int t = warp; t < a.T; t += kRouteWarps) select_token(a, t, lane);
   if (threadIdx.x == 0) *a.counter = 0u;  // leave the counter zero for the next call
+  if (a.perm_off) {
+    extern __shared__ int s_perm[];
+    __syncthreads();
+    permute_block(a.ids, a.T * a.k, a.E, a.perm_off, a.perm_sp, a.perm_pp, s_perm);
+  }
 }
 
 __global__ void __launch_bounds__(kRouteWarps * 32) route_select_kernel(RouteArgs a) {
