@@ -189,17 +189,21 @@ ftmoe_status ftmoe_route_noalloc(const ftmoe_layer_desc* desc, const uint16_t* x
 
 /* ---------------------------------------------------------------------------
  * a3  ftmoe_quantize_act - the prefill activation quantiser on its own.
- * The pages do not say how activations reach FP4 tensor cores.  The library's
- * rule, applied inside ftmoe_expert_ffn's tensor-core path to the gathered rows
- * of x and to h, is for each block of 16 consecutive elements of a row:
- *   s_code = E4M3_rn_satfinite(amax / 6)            (IEEE fp32 division)
- *   q      = E2M1_rn_satfinite(v / value(s_code))   (IEEE fp32 division),
- *            or a zero of v's sign when the scale is 0
- * with a tensor-level scale of 1.  This call applies it to x [T][d] (bf16) in
- * token order:
- *   codes   uint8 [T][d/2], element 2i in the low nibble of byte i
- *   scales  uint8 [T][d/16], E4M3 codes
- * Preconditions: 1 <= T <= 2^20, d % 256 == 0.
+ * The pages do not say how activations reach FP4 / FP8 tensor cores.  The
+ * library's rules, applied inside ftmoe_expert_ffn's tensor-core paths to the
+ * gathered rows of x (and to h), by the layer's weight format:
+ *   NVFP4     per block of 16 consecutive elements of a row:
+ *               s_code = E4M3_rn_satfinite(amax / 6)            (IEEE fp32 division)
+ *               q      = E2M1_rn_satfinite(v / value(s_code))   (IEEE fp32 division)
+ *             tensor-level scale 1;
+ *   FP8_B128  per block of 128 consecutive elements of a row:
+ *               s = amax / 448 (fp32, IEEE division),  q = E4M3_rn_satfinite(v / s)
+ * with q a zero of v's sign when the scale is 0.  This call applies the rule to
+ * x [T][d] (bf16) in token order:
+ *   NVFP4     codes uint8 [T][d/2] (element 2i in the low nibble of byte i),
+ *             scales uint8 [T][d/16] (E4M3 codes)
+ *   FP8_B128  codes uint8 [T][d] (E4M3), scales float [T][d/128] (4-byte aligned)
+ * Other formats: NVFP4's rule.  Preconditions: 1 <= T <= 2^20, d % 256 == 0.
  * ------------------------------------------------------------------------- */
 ftmoe_status ftmoe_quantize_act(const ftmoe_layer_desc* desc, const uint16_t* x, int T, uint8_t* codes,
                                 uint8_t* scales, void* stream);
@@ -243,6 +247,12 @@ ftmoe_status ftmoe_permute(const ftmoe_layer_desc* desc, const int32_t* topk_ids
  *      weights->prepared (FTMOE_ERR_INVALID_ARG without it).  With topk_w the
  *      combine is fused (fp32 atomic adds, so the order of the k adds into
  *      out varies between runs); without it y is written in sorted order.
+ *   2  FP8_B128 weights, T >= FTMOE_PREFILL_MIN_T, d % 256 == 0, ffn % 128 == 0,
+ *      d and ffn <= 8192: tcgen05 FP8 tensor cores.  x and h are quantised to
+ *      E4M3 with one fp32 scale per (row, 128 columns) (rule of
+ *      ftmoe_quantize_act); each 128-wide K step's fp32 partial is scaled by the
+ *      activation and weight block scales and accumulated in fp32.  Combine as
+ *      for path 1.  Reads the canonical arena (no preparation).
  * ------------------------------------------------------------------------- */
 #define FTMOE_PREFILL_MIN_T 256
 size_t ftmoe_expert_ffn_workspace_size(const ftmoe_layer_desc* desc, int T);

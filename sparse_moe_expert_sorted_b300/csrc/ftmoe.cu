@@ -13,6 +13,7 @@
 #include "lru.cuh"
 #include "permute.cuh"
 #include "prefill.cuh"
+#include "prefill8.cuh"
 #include "route.cuh"
 
 using namespace ftmoe;
@@ -95,7 +96,11 @@ size_t permute_ws(const ftmoe_layer_desc* d, int T) {
 }
 // --- tensor-core prefill path (NVFP4) ---------------------------------------
 int ffn_path(const ftmoe_layer_desc* d, int T) {
-  if (d->fmt == FTMOE_NVFP4 && T >= FTMOE_PREFILL_MIN_T && d->d % kStageK == 0 && d->ffn % kStageK == 0) return 1;
+  if (T < FTMOE_PREFILL_MIN_T) return 0;
+  if (d->fmt == FTMOE_NVFP4 && d->d % kStageK == 0 && d->ffn % kStageK == 0) return 1;
+  if (d->fmt == FTMOE_FP8_B128 && d->d % 256 == 0 && d->ffn % 128 == 0 && d->d / 128 <= kG8MaxKB &&
+      d->ffn / 128 <= kG8MaxKB)
+    return 2;
   return 0;
 }
 // N tile of the gate/up GEMM: NH gate rows + NH up rows
@@ -128,8 +133,27 @@ TcWs tc_ws(const ftmoe_layer_desc* d, int T) {
   return w;
 }
 
+// FP8 path: header | xq_tok [T][d] | sx_tok [T][d/128] | xq [R][d] | sx [d/128][R] | hq [R][f] | sh [f/128][R]
+struct Tc8Ws {
+  size_t rows, xq_tok, sx_tok, xq, sx, hq, sh, total;
+};
+Tc8Ws tc8_ws(const ftmoe_layer_desc* d, int T) {
+  Tc8Ws w;
+  w.rows = tc_rows_cap(d, T);
+  size_t o = align1k(kWsHeader);
+  w.xq_tok = o; o += align1k(size_t(T) * d->d);
+  w.sx_tok = o; o += align1k(size_t(T) * (d->d / 128) * 4);
+  w.xq = o; o += align1k(w.rows * d->d);
+  w.sx = o; o += align1k(w.rows * (d->d / 128) * 4);
+  w.hq = o; o += align1k(w.rows * d->ffn);
+  w.sh = o; o += align1k(w.rows * (d->ffn / 128) * 4);
+  w.total = o;
+  return w;
+}
+
 size_t ffn_ws(const ftmoe_layer_desc* d, int T) {
   if (ffn_path(d, T) == 1) return tc_ws(d, T).total;
+  if (ffn_path(d, T) == 2) return tc8_ws(d, T).total;
   const size_t P = size_t(T) * d->k;
   return kWsHeader + align256(P * d->ffn * sizeof(float));
 }
@@ -412,6 +436,87 @@ ftmoe_status ffn_tc_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, cons
 bool ffn_dec_kernel(const ftmoe_layer_desc* d, int T) {
   return ffn_path(d, T) == 0 && (d->fmt == FTMOE_NVFP4 || d->fmt == FTMOE_MXFP4);
 }
+template <int MODE>
+ftmoe_status launch_gemm8(const CUtensorMap& ta, const CUtensorMap& tb0, const CUtensorMap& tb1, const Gemm8Args& g,
+                          int max_tiles, cudaStream_t st) {
+  const int grid = std::max(1, std::min(num_sms(), max_tiles));
+  return launch(gemm8_kernel<MODE>, dim3(grid), dim3(kGemmThreads), size_t(G8Cfg<MODE>::SMEM), st, ta, tb0, tb1, g);
+}
+
+// 2D byte matrix [rows][row_bytes], boxes of 128 bytes x box_rows, 128-byte swizzle (box_rows <= 256)
+// (make_map above); FP8 path: quantise, gather, gate/up GEMM (SwiGLU + E4M3 h), down GEMM.
+ftmoe_status ffn_tc8_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of,
+                          const uint16_t* x, int T, const int32_t* off, const int32_t* sp, const float* topk_w,
+                          float* y_or_out, void* ws, float* zero_out, cudaStream_t st) {
+  const Tc8Ws L = tc8_ws(d, T);
+  char* base = static_cast<char*>(ws);
+  uint8_t* xq_tok = reinterpret_cast<uint8_t*>(base + L.xq_tok);
+  float* sx_tok = reinterpret_cast<float*>(base + L.sx_tok);
+  uint8_t* xq = reinterpret_cast<uint8_t*>(base + L.xq);
+  float* sx = reinterpret_cast<float*>(base + L.sx);
+  uint8_t* hq = reinterpret_cast<uint8_t*>(base + L.hq);
+  float* sh = reinterpret_cast<float*>(base + L.sh);
+  const int P = T * d->k;
+  const int sms = num_sms();
+  const long long qblocks = (long long)T * (d->d / 128);
+  ftmoe_status s = launch(quantize8_kernel, dim3((unsigned)std::min<long long>((qblocks + 7) / 8, sms * 16)), dim3(256),
+                          0, st, x, T, d->d, xq_tok, sx_tok);
+  if (s != FTMOE_OK) return s;
+  Gather8Args q;
+  q.xq_tok = xq_tok;
+  q.sx_tok = sx_tok;
+  q.d = d->d;
+  q.k = d->k;
+  q.E = d->E;
+  q.C = w->C;
+  q.P = P;
+  q.offsets = off;
+  q.sorted_pair = sp;
+  q.slot_of = slot_of;
+  q.xq = xq;
+  q.sx = sx;
+  q.rows_cap = int(L.rows);
+  q.zero_out = reinterpret_cast<float4*>(zero_out);
+  q.zero_n4 = zero_out ? (long long)T * d->d / 4 : 0;
+  s = launch(gather8_kernel, dim3(std::min(cdiv(L.rows, kActqWarps), sms * 8)), dim3(kActqWarps * 32), 0, st, q);
+  if (s != FTMOE_OK) return s;
+  CUtensorMap tA1, tG, tU, tA2, tD;
+  const size_t C = size_t(w->C);
+  if (!make_map(&tA1, xq, d->d, L.rows, kTileM) || !make_map(&tG, w->gate, d->d, C * d->ffn, 128) ||
+      !make_map(&tU, w->up, d->d, C * d->ffn, 128) || !make_map(&tA2, hq, d->ffn, L.rows, kTileM) ||
+      !make_map(&tD, w->down, d->ffn, C * d->d, 256))
+    return FTMOE_ERR_CUDA;
+  Gemm8Args g;
+  g.E = d->E;
+  g.k = d->k;
+  g.d = d->d;
+  g.f = d->ffn;
+  g.C = w->C;
+  g.P = P;
+  g.rows_cap = int(L.rows);
+  g.offsets = off;
+  g.sorted_pair = sp;
+  g.slot_of = slot_of;
+  g.sx = sx;
+  g.sw0 = static_cast<const float*>(w->gate_scale);
+  g.sw1 = static_cast<const float*>(w->up_scale);
+  g.hq = hq;
+  g.sh = sh;
+  g.topk_w = nullptr;
+  g.out = nullptr;
+  const int mts = int(L.rows / kTileM);
+  s = launch_gemm8<0>(tA1, tG, tU, g, mts * (d->ffn / 128), st);
+  if (s != FTMOE_OK) return s;
+  g.sx = sh;
+  g.sw0 = static_cast<const float*>(w->down_scale);
+  g.sw1 = nullptr;
+  g.hq = nullptr;
+  g.sh = nullptr;
+  g.topk_w = topk_w;
+  g.out = y_or_out;
+  return launch_gemm8<1>(tA2, tD, tD, g, mts * (d->d / 256), st);
+}
+
 ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of, const uint16_t* x,
                       int T, const int32_t* off, const int32_t* sp, const float* topk_w, float* y_or_out, void* ws,
                       void* hdr, cudaStream_t st, uint16_t* out_bf16 = nullptr) {
@@ -442,6 +547,7 @@ ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const i
                    : nullptr;
   const int P = T * d->k;
   if (ffn_path(d, T) == 1) return ffn_tc_impl(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, nullptr, st);
+  if (ffn_path(d, T) == 2) return ffn_tc8_impl(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, nullptr, st);
   switch (d->fmt) {
     case FTMOE_BF16: return ffn_stream_launch<FTMOE_BF16>(a, P, st);
     case FTMOE_NVFP4: return ffn_dec_launch<FTMOE_NVFP4>(a, P, hdr, st);
@@ -579,6 +685,12 @@ ftmoe_status ftmoe_quantize_act(const ftmoe_layer_desc* d, const uint16_t* x, in
                                 void* stream) {
   if (!desc_ok(d) || T < 1 || T > kMaxT || !x || !codes || !scales) return FTMOE_ERR_INVALID_ARG;
   if (!aligned16(x) || (reinterpret_cast<uintptr_t>(codes) & 7u)) return FTMOE_ERR_INVALID_ARG;
+  if (d->fmt == FTMOE_FP8_B128) {
+    if (reinterpret_cast<uintptr_t>(scales) & 3u) return FTMOE_ERR_INVALID_ARG;
+    const long long qblocks = (long long)T * (d->d / 128);
+    return launch(quantize8_kernel, dim3((unsigned)std::min<long long>((qblocks + 7) / 8, num_sms() * 16)), dim3(256),
+                  0, as_stream(stream), x, T, d->d, codes, reinterpret_cast<float*>(scales));
+  }
   return launch(quantize_act_kernel, dim3(std::min(cdiv(T, kActqWarps), num_sms() * 8)), dim3(kActqWarps * 32), 0,
                 as_stream(stream), x, T, d->d, codes, scales);
 }
@@ -756,9 +868,10 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
     }
   }
   if (s != FTMOE_OK) return s;
-  if (ffn_path(d, T) == 1) {
-    // tensor-core path: out_f32 is zeroed by the first FFN kernel and the down GEMM adds w * y into it
-    s = ffn_tc_impl(d, w, slot_of, x, T, off, sp, w_, out_f32, view, out_f32, st);
+  if (ffn_path(d, T) != 0) {
+    // tensor-core path: out_f32 is zeroed by the gather kernel and the down GEMM adds w * y into it
+    s = ffn_path(d, T) == 1 ? ffn_tc_impl(d, w, slot_of, x, T, off, sp, w_, out_f32, view, out_f32, st)
+                            : ffn_tc8_impl(d, w, slot_of, x, T, off, sp, w_, out_f32, view, out_f32, st);
     if (s != FTMOE_OK || !out_bf16) return s;
     return combine_impl(d, T, nullptr, pp, w_, ids_, slot_of, out_f32, out_f32, out_bf16, st);
   }

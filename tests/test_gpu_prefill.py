@@ -1,5 +1,6 @@
-"""Parity of the tensor-core prefill path (NVFP4 weights, NVFP4 activations)
-with the oracle's mirror of it.
+"""Parity of the tensor-core prefill paths with the oracle's mirror of them:
+path 1 (NVFP4 weights, NVFP4 activations) and path 2 (FP8_B128 weights, E4M3
+activations with one fp32 scale per row and 128 columns).
 
   * ftmoe_quantize_act: activation codes and scales bit for bit, including
     zero blocks, signed zeros, blocks whose scale underflows to 0, exact
@@ -9,7 +10,9 @@ with the oracle's mirror of it.
     M-tiles with ragged tails, both N tilings of gate/up (96 + 96 and 64 + 64),
     slot indirection, empty experts and skewed routing;
   * the exact split of the resident set (A + B = full, reassociation only);
-  * the layer call (route + permute + FFN + fused combine + bf16).
+  * the layer call (route + permute + FFN + fused combine + bf16);
+  * the same for path 2: E4M3 activation codes and scales bit for bit, parity
+    over several K steps and M tiles with skew, the exact split.
 """
 import numpy as np
 import pytest
@@ -144,3 +147,74 @@ def test_prefill_path_needs_prepared_scales():
     off, sp, pp = permute(dsc, ids)
     with pytest.raises(ft.FtmoeError):
         expert_ffn(dsc, W, None, x, off, sp)
+
+
+# ---------------------------------------------------------------------------
+# FP8_B128 weights: path 2 (E4M3 activations, one fp32 scale per row and 128 columns)
+# ---------------------------------------------------------------------------
+def test_quantize_act_fp8_is_bit_exact():
+    d, T = 512, 40
+    x = synth.make_x(T, d, 21).float().numpy()
+    x[0] = 0.0
+    x[1] = -0.0
+    x[2, :128] = 1e-38                                           # scale underflows towards zero
+    x[3, :128] = np.linspace(-448.0, 448.0, 128)                 # scale exactly 1
+    x[4] = 3e4 * np.sign(x[4])
+    xb = _bf16(x)
+    dsc = ft.desc(8, 2, d, 256, ft.FP8_B128)
+    codes = torch.empty(T, d, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(T, d // 128, dtype=torch.float32, device="cuda")
+    ft.quantize_act(dsc, xb.cuda(), codes, scales.view(torch.uint8))
+    q, s = F.quant_act_fp8(F.bf16_to_f32(bf16_bits(xb)))
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), np.asarray(s, np.float32).view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy(), q)
+
+
+FP8_CASES = [
+    # E, k, d, f, T, zipf
+    (16, 4, 512, 256, 512, 0.0),
+    (8, 2, 768, 384, 300, 0.0),      # 6 and 3 K steps, ragged tail
+    (32, 6, 256, 512, 700, 1.2),     # skewed: several M tiles per hot expert, empty experts
+]
+
+
+@pytest.mark.parametrize("E,k,d,f,T,zipf", FP8_CASES)
+def test_prefill_fp8_matches_mirror_oracle(E, k, d, f, T, zipf):
+    W = synth.make_experts(synth.FP8_B128, E, d, f, E + T, device="cuda")
+    x = synth.make_x(T, d, E + T)
+    wr = synth.make_router(E, d, E + T)
+    bias = synth.make_zipf_bias(E, zipf, E + T) if zipf else np.zeros(E, np.float32)
+    dsc = ft.desc(E, k, d, f, ft.FP8_B128)
+    assert ft.expert_ffn_path(dsc, T) == 2
+    slot_np = np.random.default_rng(T).permutation(E).astype(np.int32)
+    ref = OF.layer(weights_to_numpy(W), slot_np, bf16_bits(x), bf16_bits(wr), bias, k, 1, act_quant="fp8")
+    xd = x.cuda()
+    ids, w, _ = route(dsc, xd, wr.cuda(), torch.from_numpy(bias).cuda())
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    off, sp, pp = permute(dsc, ids)
+    slot = torch.from_numpy(slot_np).cuda()
+    y = expert_ffn(dsc, W, slot, xd, off, sp)
+    assert rel_l2(y.cpu().numpy(), ref["y"]) < TOL
+    out = expert_ffn(dsc, W, slot, xd, off, sp, topk_w=w)
+    assert rel_l2(out.cpu().numpy(), ref["out"]) < TOL
+    ids2, w2, of2, ob2 = layer_forward(dsc, W, slot, xd, wr.cuda(), torch.from_numpy(bias).cuda())
+    assert rel_l2(of2.cpu().numpy(), ref["out"]) < TOL
+    assert rel_l2(ob2.float().cpu().numpy(), ref["out"]) < TOL
+    assert ft.get_device_error() == 0
+
+
+def test_prefill_fp8_exact_split():
+    E, k, d, f, T = 16, 4, 512, 256, 512
+    W = synth.make_experts(synth.FP8_B128, E, d, f, 3, device="cuda")
+    x = synth.make_x(T, d, 3).cuda()
+    wr = synth.make_router(E, d, 3)
+    dsc = ft.desc(E, k, d, f, ft.FP8_B128)
+    ids, w, _ = route(dsc, x, wr.cuda())
+    off, sp, pp = permute(dsc, ids)
+    mask = synth.make_split(E, seed=2)
+    sa = torch.from_numpy(np.where(mask, np.arange(E), -1).astype(np.int32)).cuda()
+    sb = torch.from_numpy(np.where(~mask, np.arange(E), -1).astype(np.int32)).cuda()
+    full = expert_ffn(dsc, W, None, x, off, sp, topk_w=w)
+    a = expert_ffn(dsc, W, sa, x, off, sp, topk_w=w)
+    b = expert_ffn(dsc, W, sb, x, off, sp, topk_w=w)
+    assert rel_l2((a + b).cpu().numpy(), full.cpu().numpy()) <= 1e-6
