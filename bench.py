@@ -69,6 +69,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="layer copies to cycle (decode workloads; default 16)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU baseline sample")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the expert count (a smaller case of the same kernels, for profiler captures)")
     return ap.parse_args()
 
 
@@ -238,6 +240,10 @@ def bench_ours(args, rank, ws):
     wl, T, n_layers = WORKLOADS[args.workload]
     if args.layers and not args.workload.startswith("stack"):
         n_layers = args.layers
+    if args.experts:
+        import dataclasses
+        wl = dataclasses.replace(wl, layer=dataclasses.replace(wl.layer, E=args.experts),
+                                 capacity=min(wl.capacity, args.experts) if wl.capacity else 0)
     L = wl.layer
     dev = "cuda"
     dsc = ft.desc(L.E, L.k, L.d, L.f, L.fmt, L.renorm)
@@ -391,7 +397,7 @@ def bench_ours(args, rank, ws):
     achieved = alg_bytes / (ffn_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                 "frac": round(achieved / hbm, 4), "traffic": ncu_traffic(args.workload),
-                "kernel": "ftmoe_expert_ffn (gate/up + down kernels)", "peak_source": src,
+                "kernel": "ftmoe_expert_ffn (decode: sd_ffn_kernel, one launch)", "peak_source": src,
                 "ffn_us": round(ffn_ms * 1e3, 3), "alg_bytes_per_call": int(alg_bytes),
                 "mean_unique_experts": round(float(np.mean(uniq)), 2)}
     if path != 0:
@@ -401,7 +407,8 @@ def bench_ours(args, rank, ws):
         ach = flops / (ffn_ms / 1e3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(ach, 1), "peak": round(peak_t, 1), "unit": "TFLOP/s",
                     "frac": round(ach / peak_t, 4), "traffic": ncu_traffic(args.workload),
-                    "kernel": "ftmoe_expert_ffn", "peak_source": f"{src} bf16 x {ratio:g} (nominal ratio)",
+                    "kernel": "ftmoe_expert_ffn (quantise, gather, gate/up GEMM, down GEMM)",
+                    "peak_source": f"{src} bf16 x {ratio:g} (nominal ratio)",
                     "ffn_us": round(ffn_ms * 1e3, 3)}
 
     # --- end to end through the public API with host buffers ------------------
@@ -412,7 +419,8 @@ def bench_ours(args, rank, ws):
         "warmup": args.warmup, "ms_per_step": round(ms_max / K, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": {0: "bf16", 1: "nvfp4", 2: "mxfp4", 3: "fp8_e4m3"}[L.fmt] + " weights, fp32 accumulate",
         "data": "synthetic (seeded; random-init weights)",
-        "config": {"workload": f"{wl.name} T={T}" + (" x8 layers" if stack else ""), "E": L.E, "k": L.k,
+        "config": {"workload": f"{wl.name} T={T}" + (" x8 layers" if stack else "") +
+                               (f" (E overridden to {L.E})" if args.experts else ""), "E": L.E, "k": L.k,
                    "d": L.d, "ffn": L.f, "tokens_per_step": T, "layers_cycled": n_layers,
                    "l2": f"weights > L2: {n_layers} distinct layer copies cycled "
                          f"({n_layers * L.E * eb / 1e9:.1f} GB)",
