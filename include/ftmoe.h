@@ -21,9 +21,11 @@
  *     owns all memory.  The library never allocates or frees caller memory.
  *   - Scratch is passed as (ws, ws_bytes).  Its size comes from the matching
  *     *_workspace_size query.  Before its first use, the workspace's first
- *     FTMOE_WS_ZERO_BYTES bytes must be zero.  Every call leaves them zero
- *     again (they hold completion counters).  One workspace must not be used by
- *     two calls that can run at the same time.
+ *     FTMOE_WS_ZERO_BYTES bytes must be zero.  They hold the library's
+ *     completion and grid-sync counters from call to call: the caller must not
+ *     write them afterwards, except to zero them again after a call reported
+ *     FTMOE_ERR_TIMEOUT.  One workspace must not be used by two calls that can
+ *     run at the same time.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
  *     asynchronous on it.  Kernels are launched with programmatic dependent
  *     launch, so consecutive calls on one stream overlap their launch latency.
@@ -327,13 +329,25 @@ ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* lru, const int32_t* trace, int ste
                                    int64_t* counters, void* stream);
 
 /* ---------------------------------------------------------------------------
- * Whole layer in one call: route -> permute -> expert FFN (fused combine) -> bf16.
+ * Whole layer in one call: route -> permute -> expert FFN -> combine -> bf16.
  * This is the same work as the four calls above, on one workspace.
  *   slot_of    int32 [E] or NULL (every expert resident in slot e)
  *   topk_ids, topk_w  outputs as in ftmoe_route (may be NULL only together)
- *   out_f32    fp32 [T][d] (required: the accumulator);  out_bf16  bf16 [T][d] or NULL
+ *   out_f32    fp32 [T][d] (required);  out_bf16  bf16 [T][d] or NULL
+ * Two forms (ftmoe_layer_path tells which one a call takes):
+ *   1  one kernel, for T <= 8 with NVFP4 or MXFP4 weights and weights->prepared:
+ *      every CTA computes the logits of its share of the experts, one grid-wide
+ *      sync, then every CTA selects the top-k and sorts the pairs itself and
+ *      streams its share of the selected experts.  The combine is a merge in
+ *      ascending rank, as ftmoe_combine computes it, so the results equal the
+ *      separate calls' bit for bit.
+ *   0  the separate steps on one stream (the expert FFN with fused combine on
+ *      the decode path, the combine call otherwise).
  * ------------------------------------------------------------------------- */
 size_t ftmoe_layer_workspace_size(const ftmoe_layer_desc* desc, int T);
+/* 1 = ftmoe_layer_forward runs as one kernel for these weights and T, 0 = as separate
+ * steps, -1 = invalid descriptor or weights. */
+int ftmoe_layer_path(const ftmoe_layer_desc* desc, const ftmoe_weights* weights, int T);
 ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* desc, const ftmoe_weights* weights,
                                  const int32_t* slot_of, const uint16_t* x, const uint16_t* w_router,
                                  const float* logit_bias, int T, int32_t* topk_ids, float* topk_w,

@@ -31,7 +31,7 @@ EXPORTS = [
     "ftmoe_prepare_weights_size", "ftmoe_prepare_weights", "ftmoe_quantize_act",
     "ftmoe_expert_ffn_workspace_size", "ftmoe_expert_ffn_path", "ftmoe_expert_ffn", "ftmoe_combine", "ftmoe_lru_create", "ftmoe_lru_reset",
     "ftmoe_lru_destroy", "ftmoe_lru_slot_of", "ftmoe_lru_copy_slot_of", "ftmoe_slot_lru", "ftmoe_slot_lru_replay",
-    "ftmoe_layer_workspace_size", "ftmoe_layer_forward", "ftmoe_status_string", "ftmoe_get_device_error",
+    "ftmoe_layer_workspace_size", "ftmoe_layer_path", "ftmoe_layer_forward", "ftmoe_status_string", "ftmoe_get_device_error",
     "ftmoe_version",
 ]
 
@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
         "ftmoe_slot_lru": (_I, [_P, _I, _P, _I, _I, _P, _P, _P, _P, _P]),
         "ftmoe_slot_lru_replay": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, ctypes.c_int64, _P, _P]),
         "ftmoe_layer_workspace_size": (_SZ, [_P, _I]),
+        "ftmoe_layer_path": (_I, [_P, _P, _I]),
         "ftmoe_layer_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
         "ftmoe_status_string": (ctypes.c_char_p, [_I]),
         "ftmoe_get_device_error": (_I, [ctypes.POINTER(_I), _P]),
@@ -239,6 +240,11 @@ def combine(dsc, T, y, pair_pos, topk_w, topk_ids, slot_of, partial_b, out_f32, 
 
 def layer_workspace_size(dsc: LayerDesc, T: int) -> int:
     return lib().ftmoe_layer_workspace_size(ctypes.byref(dsc), T)
+
+
+def layer_path(dsc: LayerDesc, wstruct, T: int) -> int:
+    """1 = ftmoe_layer_forward runs as one kernel (router + expert FFN + merge), 0 = as separate steps."""
+    return lib().ftmoe_layer_path(ctypes.byref(dsc), ctypes.byref(wstruct), T)
 
 
 def layer_forward(dsc, wstruct, slot_of, x, w_router, bias, ids, topk_w, out_f32, out_bf16, ws, stream=None):

@@ -44,6 +44,9 @@ constexpr size_t kWsCounterRoute = 0;     // uint32
 constexpr size_t kWsCounterPermute = 4;   // uint32
 constexpr size_t kWsBarrierCount = 16;    // uint32: grid barrier arrivals (back to 0 after each barrier)
 constexpr size_t kWsBarrierGen = 20;      // uint32: grid barrier generation (only ever incremented)
+// uint64: arrivals of the grid syncs of kernels whose grid is exactly one CTA per SM.  Only
+// ever incremented, so it stays a multiple of that grid size between syncs.
+constexpr size_t kWsGridSync = 24;
 constexpr size_t kWsHeader = FTMOE_WS_ZERO_BYTES;
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 

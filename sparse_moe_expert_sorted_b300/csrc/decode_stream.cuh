@@ -1,6 +1,6 @@
-// a4 (+a5) decode path for NVFP4 / MXFP4, streaming form: the selected experts'
-// weights flow through a shared-memory ring filled by bulk copies, and
-// consumer warps run the warp-level MMAs of decode.cuh on them.
+// a4 (+a5, and a1 + a2 in the layer call) decode path for NVFP4 / MXFP4, streaming
+// form: the selected experts' weights flow through a shared-memory ring filled by bulk
+// copies, and consumer warps run the warp-level MMAs of decode.cuh on them.
 //
 // Pages: resident experts are computed on GPU tensor cores from expert slots
 // (zubnet.ai, "FreeToken, Unsloth GGUF ... consumer hardware"); in decode a
@@ -14,11 +14,11 @@
 //                prepared decode layout (below) is contiguous.  Few large copies
 //                keep the copy engine's per-copy cost small.
 //   warps 1-16   consumers: MMAs on the staged rows against the tokens staged
-//                in shared memory as f16; partials of the 8 warps meet in
-//                shared memory; epilogue.
+//                in shared memory as f16.
+//   warp 17      epilogue: reduces the consumers' partial sums and writes h or y.
 // Work items, in order: phase A (gate/up) then phase B (down).  An item is
-// (expert, group of up to 8 tokens, block of rows); a stage is one item's rows.  Each CTA takes a contiguous
-// range of items, so consecutive items share the staged tokens.
+// (expert, group of up to 8 tokens, block of rows); a stage is one item's rows.  Each CTA
+// takes a contiguous range of items, so consecutive items share the staged tokens.
 //   phase A item: 16 gate + 16 up rows; the consumer warps split K.
 //   phase B item: 32 down rows; consumer warp w takes row tile w & 1 and K part w >> 1.
 // Prepared decode layout (ftmoe_prepare_weights), per slot: phase-A tiles (16 gate
@@ -28,9 +28,26 @@
 // phase-A tile is [gate codes][up codes][gate scales][up scales].  In this order the
 // 8 rows of an MMA fragment load sit side by side, so every shared-memory fragment read
 // covers contiguous 128-byte lines (no bank conflicts).
-// Between the phases the consumers meet at a grid barrier (every h written);
-// the producer does not wait there, so the first down weights are already in
-// flight.  The layer call also zeroes out first and casts it to bf16 last.
+//
+// Cross-warp reduction without a CTA barrier: each consumer warp writes its partial
+// sums of an item into one of two reduction buffers (item parity) and counts itself in,
+// then goes on to the next item.  The epilogue warp waits for the 16 counts, sums the
+// partials in warp order (results do not depend on timing), writes h or y and frees the
+// buffer.  h is kept as f16 (the precision the down MMA reads it in).
+//
+// Between the phases: ftmoe_expert_ffn meets at a grid sync (every h written).  The layer
+// call (ROUTE) instead counts the finished gate/up items of each expert, and a down item
+// waits only for its own expert.  The producer never waits there, so the first down
+// weights are already in flight.
+//
+// ROUTE (ftmoe_layer_forward with few tokens): the router, top-k and expert sort run in
+// the same kernel.  Before its programmatic-launch wait each CTA copies the router rows
+// of its experts (e = CTA, CTA + grid, ...) to shared memory (weights only); it then
+// computes their logits in the router's fixed order R, and after one grid sync every CTA
+// selects the top-k of all tokens itself (a rank count in shared memory) and sorts the
+// pairs by expert.  The combine is a merge: the down epilogue writes y per pair; the last
+// of a token's resident pairs to finish a 32-column block sums w * y over the token's
+// ranks in ascending order (as ftmoe_combine does) and writes out in fp32 and bf16.
 #pragma once
 #include "decode.cuh"
 #include "tc.cuh"
@@ -38,11 +55,13 @@
 namespace ftmoe {
 
 constexpr int kSdCons = 16;                    // consumer warps
-constexpr int kSdThreads = (1 + kSdCons) * 32;
+constexpr int kSdEpiWarp = 1 + kSdCons;        // the epilogue warp (after producer and consumers)
+constexpr int kSdThreads = (2 + kSdCons) * 32;
 constexpr int kSdRowsA = 16;                   // gate (and up) rows per phase-A item
 constexpr int kSdRowsB = 32;                   // down rows per phase-B item
-// per-expert info: item starts (A, B), first row, rows, slot, tensor scales (3); then the token group
-__host__ __device__ inline int sd_info_ints(int E) { return 8 * (E + 8) + 32; }
+// per-expert info: item starts (A, B), first row, rows, slot, tensor scales (3); then the token
+// group (token, weight and pair of each row, 8 each) and the scan's chunk totals (2 x 32)
+__host__ __device__ inline int sd_info_ints(int E) { return 8 * (E + 8) + 96; }
 
 // Bytes of one prepared tile: phase A (16 gate + 16 up rows, K = d), phase B (32 down rows, K = f).
 __host__ __device__ inline int sd_block_bytes_a(int d, int fmt) {
@@ -105,69 +124,87 @@ __global__ void prep_decode_kernel(const uint8_t* gate, const uint8_t* up, const
   }
 }
 
+constexpr int kSdMaxStages = 6;
+constexpr int kSdRedBufs = 2;       // reduction buffers at most (items alternate between them)
+constexpr int kSdRouteMaxT = 8;     // tokens the fused router takes (one token group per expert)
+
 // Layout of one stage and of the kernel's shared memory, for one (d, f, format).  A stage
-// holds whole rows (K = d in phase A, f in phase B), so each matrix tile is one contiguous
-// run of the canonical layout and lands with one bulk copy: codes [rows][K/2], then
-// scales [rows][K/16 or K/32].
+// holds one item's tile (whole rows: K = d in phase A, f in phase B), which lands with one
+// bulk copy.
 struct SdLayout {
-  int kcA, nkA, kcB, nkB;     // K per stage and stages per item, phase A (K = d) and B (K = f)
-  int csA, ssA, csB, ssB;     // code / scale row strides in the stage (bytes)
   int stage_bytes, stages;
   int xrows, estride;         // staged token rows; per-expert info stride (ints)
-  int off_x, off_red, off_rank, off_bar, smem;
+  int nred;                   // floats per reduction buffer: [warp][m 2][row 16][xrows]
+  int nbufs;                  // reduction buffers: 2, or 1 where two would leave fewer than 2 stages
+  int route_ints;             // fused router scratch (0 without it)
+  int off_x, off_red, off_rank, off_route, off_bar, smem;
 };
 
-// xrows: tokens staged at once (min(8, T))
-__host__ __device__ inline SdLayout sd_layout(int E, int d, int f, int fmt, int xrows, int max_smem) {
+// fused router scratch: logits [T][E], ids/values/weights/resident flags/sorted pairs [T*k], expected merges [T], offsets [E+1]
+__host__ __device__ inline int sd_route_ints(int E, int T, int k) { return T * E + 5 * T * k + T + E + 1; }
+
+// T: tokens of the call (xrows = min(8, T)); route: with the fused router
+__host__ __device__ inline SdLayout sd_layout(int E, int d, int f, int fmt, int T, int k, bool route, int max_smem) {
   SdLayout L;
-  L.xrows = xrows;
+  L.xrows = T < 8 ? T : 8;
   L.estride = E + 8;
-  const int sdiv = fmt == FTMOE_NVFP4 ? 16 : 32;
-  L.kcA = d;
-  L.nkA = 1;
-  L.kcB = f;
-  L.nkB = 1;
-  L.csA = d / 2;
-  L.ssA = d / sdiv;
-  L.csB = f / 2;
-  L.ssB = f / sdiv;
   const int sa = sd_block_bytes_a(d, fmt), sb = sd_block_bytes_b(f, fmt);
   L.stage_bytes = ((sa > sb ? sa : sb) + 127) / 128 * 128;
   const int kx = d > f ? d : f;
-  const int xbytes = (xrows * (kx + 8) * 2 + 127) / 128 * 128;
-  const int red = kSdCons * 2 * 16 * 8 * 4;
-  const int fixed = xbytes + red + sd_info_ints(E) * 4 + 256;
-  L.stages = (max_smem - 1024 - fixed) / L.stage_bytes;
-  if (L.stages > 4) L.stages = 4;
+  const int xbytes = (L.xrows * (kx + 8) * 2 + 127) / 128 * 128;
+  L.nred = kSdCons * 2 * 16 * L.xrows;
+  const int info = (sd_info_ints(E) * 4 + 15) / 16 * 16;
+  L.route_ints = route ? sd_route_ints(E, T, k) : 0;
+  const int rbytes = (L.route_ints * 4 + 15) / 16 * 16;
+  int red = 0;
+  for (L.nbufs = kSdRedBufs; L.nbufs >= 1; --L.nbufs) {
+    red = L.nbufs * L.nred * 4;
+    L.stages = (max_smem - 1024 - (xbytes + red + info + rbytes + 256)) / L.stage_bytes;
+    if (L.stages >= 2 || L.nbufs == 1) break;
+  }
+  if (L.stages > kSdMaxStages) L.stages = kSdMaxStages;
   L.off_x = L.stages * L.stage_bytes;
   L.off_red = L.off_x + xbytes;
   L.off_rank = L.off_red + red;
-  L.off_bar = L.off_rank + (sd_info_ints(E) * 4 + 15) / 16 * 16;
+  L.off_route = L.off_rank + info;
+  L.off_bar = L.off_route + rbytes;
   L.smem = L.off_bar + 256 + 128;
   return L;
 }
 
-// Whether the streaming kernel takes this shape: E <= 512 and at least 2 stages of
+// Whether the streaming kernel takes this shape: E <= 1024 and at least 2 stages of
 // shared memory.  (Every tile copy is a multiple of 16 bytes at a 16-byte boundary:
 // d and f are multiples of 128.)
-__host__ inline bool sd_supported(int E, int d, int f, int fmt, int xrows, int max_smem) {
+__host__ inline bool sd_supported(int E, int d, int f, int fmt, int T, int k, int max_smem) {
   if (fmt != FTMOE_NVFP4 && fmt != FTMOE_MXFP4) return false;
   if (E > 1024) return false;
-  return sd_layout(E, d, f, fmt, xrows, max_smem).stages >= 2;
+  return sd_layout(E, d, f, fmt, T, k, false, max_smem).stages >= 2;
+}
+// Whether the layer call can fuse the router: T <= 8, the rank count small
+// (T * E * E <= 2^22 compares), and this CTA's router rows fit in the ring.
+__host__ inline bool sd_route_supported(int E, int d, int f, int fmt, int T, int k, int grid, int max_smem) {
+  if (fmt != FTMOE_NVFP4 && fmt != FTMOE_MXFP4) return false;
+  if (E > 1024 || T < 1 || T > kSdRouteMaxT || (long long)T * E * E > (1ll << 22)) return false;
+  const SdLayout L = sd_layout(E, d, f, fmt, T, k, true, max_smem);
+  if (L.stages < 2) return false;
+  const long long rows = (E + grid - 1) / grid;
+  return rows * d * 2 <= (long long)L.stages * L.stage_bytes;
 }
 
 // items per resident expert: rows-blocks x token groups
 __device__ __forceinline__ int sd_groups(int cnt, int xrows) { return (cnt + xrows - 1) / xrows; }
 
 // s_a[e], s_b[e]: first phase-A / phase-B item of expert e; totals in s_a[E], s_b[E].
-// s_lo, s_cnt, s_slot: the expert's first sorted row, rows and slot.  All threads of the CTA.
-__device__ __forceinline__ void sd_items(const FfnArgs& a, int xrows, int* s_a, int* s_b, int* s_lo, int* s_cnt,
-                                         int* s_slot, float* s_ts) {
+// s_lo, s_cnt, s_slot: the expert's first sorted row, rows and slot (slot_src: the slot table,
+// global or a shared copy, or nullptr = slot e).  s_scan: 64 ints of scratch.  All threads.
+// The tensor scales are left to sd_tensor_scales (they are needed only by the epilogues).
+__device__ __forceinline__ void sd_items(const FfnArgs& a, const int32_t* offsets, const int32_t* slot_src, int xrows,
+                                         int* s_a, int* s_b, int* s_lo, int* s_cnt, int* s_slot, int* s_scan) {
   const int ua = a.f / kSdRowsA, ub = a.d / kSdRowsB;
   for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
-    const int lo = a.offsets[e];
-    const int cnt = a.offsets[e + 1] - lo;
-    int slot = a.slot_of ? a.slot_of[e] : e;
+    const int lo = offsets[e];
+    const int cnt = offsets[e + 1] - lo;
+    int slot = slot_src ? slot_src[e] : e;
     if (slot >= a.C) {
       if (cnt > 0 && blockIdx.x == 0) set_dev_err(DEV_ERR_BAD_SLOT);
       slot = -1;
@@ -175,64 +212,116 @@ __device__ __forceinline__ void sd_items(const FfnArgs& a, int xrows, int* s_a, 
     s_lo[e] = lo;
     s_cnt[e] = cnt;
     s_slot[e] = slot;
-#pragma unroll
-    for (int m = 0; m < 3; ++m) s_ts[3 * e + m] = (a.tscale && slot >= 0) ? a.tscale[slot * 3 + m] : 1.f;
     const int gr = (cnt > 0 && slot >= 0) ? sd_groups(cnt, xrows) : 0;
     s_a[e] = gr * ua;
     s_b[e] = gr * ub;
   }
   __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int ra = 0, rb = 0;
-    for (int base = 0; base < a.E; base += 32) {
-      const int e = base + lane;
-      const int na = e < a.E ? s_a[e] : 0, nb = e < a.E ? s_b[e] : 0;
-      int ia = na, ib = nb;
+  // exclusive scan of s_a and s_b: each warp scans 32-expert chunks, then the chunk totals
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int nch = (a.E + 31) / 32;
+  for (int c = warp; c < nch; c += nw) {
+    const int e = c * 32 + lane;
+    const int na = e < a.E ? s_a[e] : 0, nb = e < a.E ? s_b[e] : 0;
+    int ia = na, ib = nb;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int oa = __shfl_up_sync(0xFFFFFFFFu, ia, off), ob = __shfl_up_sync(0xFFFFFFFFu, ib, off);
-        if (lane >= off) {
-          ia += oa;
-          ib += ob;
-        }
+    for (int off = 1; off < 32; off <<= 1) {
+      const int oa = __shfl_up_sync(0xFFFFFFFFu, ia, off), ob = __shfl_up_sync(0xFFFFFFFFu, ib, off);
+      if (lane >= off) {
+        ia += oa;
+        ib += ob;
       }
-      if (e < a.E) {
-        s_a[e] = ra + ia - na;
-        s_b[e] = rb + ib - nb;
-      }
-      ra += __shfl_sync(0xFFFFFFFFu, ia, 31);
-      rb += __shfl_sync(0xFFFFFFFFu, ib, 31);
     }
-    if (lane == 0) {
-      s_a[a.E] = ra;
-      s_b[a.E] = rb;
+    if (e < a.E) {
+      s_a[e] = ia - na;
+      s_b[e] = ib - nb;
+    }
+    if (lane == 31) {
+      s_scan[c] = ia;
+      s_scan[32 + c] = ib;
     }
   }
   __syncthreads();
+  if (warp == 0) {
+    const int ta = lane < nch ? s_scan[lane] : 0, tb = lane < nch ? s_scan[32 + lane] : 0;
+    int ia = ta, ib = tb;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int oa = __shfl_up_sync(0xFFFFFFFFu, ia, off), ob = __shfl_up_sync(0xFFFFFFFFu, ib, off);
+      if (lane >= off) {
+        ia += oa;
+        ib += ob;
+      }
+    }
+    __syncwarp();
+    if (lane < nch) {
+      s_scan[lane] = ia - ta;
+      s_scan[32 + lane] = ib - tb;
+    }
+    if (lane == 31) {
+      s_a[a.E] = ia;
+      s_b[a.E] = ib;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+    s_a[e] += s_scan[e >> 5];
+    s_b[e] += s_scan[32 + (e >> 5)];
+  }
+  __syncthreads();
+}
+
+// Tensor scales of the experts that have items (threads i0, i0 + step, ...).
+__device__ __forceinline__ void sd_tensor_scales(const FfnArgs& a, const int* s_a, const int* s_slot, float* s_ts,
+                                                 int i0, int step) {
+  for (int e = i0; e < a.E; e += step) {
+    if (s_a[e + 1] > s_a[e]) {
+      const int slot = s_slot[e];
+#pragma unroll
+      for (int m = 0; m < 3; ++m) s_ts[3 * e + m] = a.tscale ? a.tscale[slot * 3 + m] : 1.f;
+    }
+  }
 }
 
 struct SdItem {
   int e, slot, lo, cnt, grp, n0;   // expert, slot, first sorted row, tokens, token group, row block
 };
-// Items of one CTA are visited in increasing order; *e tracks the expert (start it at -1).
-__device__ __forceinline__ SdItem sd_item(const int* s_start, const int* s_lo, const int* s_cnt, const int* s_slot,
-                                          int E, int item, int blocks, int* e) {
-  if (*e < 0) *e = find_expert(s_start, E, item);
-  while (item >= s_start[*e + 1]) ++*e;
-  SdItem it;
-  it.e = *e;
-  const int local = item - s_start[it.e];
-  it.grp = local / blocks;
-  it.n0 = local % blocks;
+// Walks a CTA's items in increasing order without divisions: `it` holds the current item
+// (expert e, token group grp, row block n0 < blocks); sd_item_first places it on the first
+// item, sd_item_next moves it to the following one.
+__device__ __forceinline__ void sd_item_load(SdItem& it, const int* s_lo, const int* s_cnt, const int* s_slot) {
   it.slot = s_slot[it.e];
   it.lo = s_lo[it.e];
   it.cnt = s_cnt[it.e];
-  return it;
+}
+__device__ __forceinline__ void sd_item_first(SdItem& it, const int* s_start, const int* s_lo, const int* s_cnt,
+                                              const int* s_slot, int E, int item, int blocks) {
+  it.e = find_expert(s_start, E, item);
+  while (item >= s_start[it.e + 1]) ++it.e;
+  const int local = item - s_start[it.e];
+  it.grp = local / blocks;
+  it.n0 = local - it.grp * blocks;
+  sd_item_load(it, s_lo, s_cnt, s_slot);
+}
+__device__ __forceinline__ void sd_item_next(SdItem& it, const int* s_start, const int* s_lo, const int* s_cnt,
+                                             const int* s_slot, int item, int blocks) {
+  if (item < s_start[it.e + 1]) {
+    if (++it.n0 == blocks) {
+      it.n0 = 0;
+      ++it.grp;
+    }
+    return;
+  }
+  do {
+    ++it.e;
+  } while (item >= s_start[it.e + 1]);
+  it.grp = 0;
+  it.n0 = 0;
+  sd_item_load(it, s_lo, s_cnt, s_slot);
 }
 
-// Consumer-only barrier (named barrier 1, the 8 consumer warps).
-__device__ __forceinline__ void sd_cons_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kSdCons * 32) : "memory"); }
+// Barrier of the consumer warps and the epilogue warp (named barrier 1; the producer is not in it).
+__device__ __forceinline__ void sd_work_sync() { asm volatile("bar.sync 1, %0;" ::"r"((kSdCons + 1) * 32) : "memory"); }
 
 // MMAs of NT 16-row tiles (NT = 2: gate and up, sharing the token fragments) over
 // super-blocks [sb_lo, sb_hi) of a staged tile.  Tile m: codes at cbase[m], scales at
@@ -315,13 +404,219 @@ __device__ __forceinline__ void sd_tiles_mma(const uint8_t* const (&cbase)[NT], 
   }
 }
 
-template <int FMT>
+// Fused router and merge of the layer call (ROUTE): router, outputs and workspace.
+struct SdRoute {
+  const uint16_t* wr;    // [E][d] bf16 router weights
+  const float* bias;     // [E] or nullptr
+  int renorm;
+  float* logits;         // [T][E] workspace
+  int32_t* ids;          // [T][k] out
+  float* tw;             // [T][k] out
+  unsigned* ready;       // [E] workspace: finished gate/up items per expert (zeroed by the kernel)
+  unsigned* merge;       // [T][d/32] workspace: finished down blocks per (token, 32 columns) (zeroed likewise)
+  float* ybuf;           // [T*k][d] workspace: y of each (token, rank) pair
+  float* out_f32;        // [T][d]
+  uint16_t* out_bf16;    // [T][d] or nullptr
+};
+
+__device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long* p, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+// Release add without a result: the earlier writes of this thread (and those ordered before
+// it by a __syncwarp) are visible before the add; the issuing warp does not wait.
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid sync of a kernel whose grid is one CTA per SM (one thread per CTA calls it).  The
+// arrival counter only grows and is a multiple of the grid size between syncs, so this
+// sync ends when it reaches the next multiple.  false = gave up (time limit or abort).
+__device__ __forceinline__ bool grid_sync_mono(unsigned long long* w, volatile int* abort) {
+  const unsigned long long G = gridDim.x;
+  const unsigned long long old = atom_add_release_u64(w, 1ull);
+  const unsigned long long target = (old / G + 1) * G;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 0; ld_acquire_u64(w) < target; ++it) {
+    if ((it & 63u) == 63u) {
+      if (abort && *abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+  return true;
+}
+
+// Waits until *v >= target (bounded); false = gave up.
+__device__ __forceinline__ bool wait_count(const unsigned* v, unsigned target, volatile int* abort) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 0; ld_acquire_u32(v) < target; ++it) {
+    if ((it & 63u) == 63u) {
+      if (abort && *abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+  return true;
+}
+
+// Waits until the shared word *v equals want (bounded); false = gave up.  Whole warp: one
+// lane polls; warp-uniform result.
+__device__ __forceinline__ bool wait_smem_eq(volatile int* v, int want, volatile int* abort) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0 && *v != want) {
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 0; *v != want; ++it) {
+      if ((it & 63u) == 63u) {
+        if (*abort || globaltimer_ns() - t0 > kWaitLimitNs) {
+          ok = 0;
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+// Router logits of this CTA's experts e = b, b + G, ... for all T tokens, in order R (the
+// router's fixed fp32 order: lane j adds the products of its 8-element chunks j, j + 32, ...
+// in ascending element order, unfused; lanes combine by a xor butterfly 16 .. 1; bias last).
+// Router rows are in shared memory (srow), x is read from global memory.  Consumer warps.
+__device__ __forceinline__ void sd_route_logits(const FfnArgs& a, const SdRoute& r, const uint8_t* srow, int ne,
+                                                int cw, int lane) {
+  const int S = a.d >> 8;    // chunks per lane
+  for (int item = cw; item < ne * a.T; item += kSdCons) {
+    const int i = item / a.T, t = item - i * a.T;
+    const int e = blockIdx.x + i * gridDim.x;
+    const uint4* wrow = reinterpret_cast<const uint4*>(srow + size_t(i) * a.d * 2);
+    const uint4* xr = reinterpret_cast<const uint4*>(a.x + size_t(t) * a.d);
+    float acc = 0.f;
+    for (int s0 = 0; s0 < S; s0 += 8) {
+      uint4 xv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) xv[q] = __ldg(xr + min(s0 + q, S - 1) * 32 + lane);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (s0 + q < S) {
+          const uint4 wv = wrow[(s0 + q) * 32 + lane];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint32_t ww = (&wv.x)[u >> 1], xx = (&xv[q].x)[u >> 1];
+            const float wf = (u & 1) ? bf16_hi(ww) : bf16_lo(ww);
+            const float xf = (u & 1) ? bf16_hi(xx) : bf16_lo(xx);
+            acc = __fadd_rn(acc, __fmul_rn(xf, wf));
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, off));
+    if (lane == 0) {
+      if (r.bias) acc = __fadd_rn(acc, r.bias[e]);
+      r.logits[size_t(t) * a.E + e] = acc;
+    }
+  }
+}
+
+// Top-k of every token by (logit desc, id asc; NaN last), softmax weights, and the stable
+// sort of the pairs by expert, all in shared memory (every CTA computes the same).  All
+// threads; ends with __syncthreads.  CTA 0 writes ids and weights.
+__device__ __forceinline__ void sd_route_select(const FfnArgs& a, const SdRoute& r, float* s_logit, int* s_ids,
+                                                float* s_val, float* s_wt, int* s_sp, int* s_off) {
+  const int T = a.T, E = a.E, k = a.k, P = T * k;
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < T * E; i += nt) s_logit[i] = __ldcg(r.logits + i);
+  __syncthreads();
+  // rank of (t, e) = experts that come before it; the first k ranks are the selection
+  for (int i = tid; i < T * E; i += nt) {
+    const int t = i / E, e = i - t * E;
+    const float v = s_logit[i];
+    const float* row = s_logit + t * E;
+    int rank = 0;
+    if (!isnan(v)) {
+      if ((E & 3) == 0 && ((t * E) & 3) == 0) {
+        const float4* r4 = reinterpret_cast<const float4*>(row);
+#pragma unroll 4
+        for (int j4 = 0; j4 < E / 4; ++j4) {
+          const float4 u = r4[j4];
+          const int j = 4 * j4;
+          rank += ((u.x > v) || (u.x == v && j < e)) + ((u.y > v) || (u.y == v && j + 1 < e)) +
+                  ((u.z > v) || (u.z == v && j + 2 < e)) + ((u.w > v) || (u.w == v && j + 3 < e));
+        }
+      } else {
+        for (int j = 0; j < E; ++j) {
+          const float u = row[j];
+          rank += (u > v) || (u == v && j < e);
+        }
+      }
+    } else {
+      for (int j = 0; j < E; ++j) rank += !isnan(row[j]) || j < e;
+    }
+    if (rank < k) {
+      s_ids[t * k + rank] = e;
+      s_val[t * k + rank] = v;
+    }
+  }
+  __syncthreads();
+  // weights: warp t, the same arithmetic as the router's select step
+  for (int t = warp; t < T; t += nt >> 5) {
+    const float m = s_val[t * k];
+    float part = 0.f;
+    if (r.renorm) {
+      part = lane < k ? expf(s_val[t * k + lane] - m) : 0.f;
+    } else {
+      for (int e = lane; e < E; e += 32) part += expf(s_logit[t * E + e] - m);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
+    if (lane < k) {
+      const float w = expf(s_val[t * k + lane] - m) / part;
+      s_wt[t * k + lane] = w;
+      if (blockIdx.x == 0) {
+        r.ids[t * k + lane] = s_ids[t * k + lane];
+        r.tw[t * k + lane] = w;
+      }
+    }
+  }
+  // expert offsets (pairs with a smaller id), then positions (stable within an expert)
+  for (int e = tid; e <= E; e += nt) {
+    int c = 0;
+    for (int p = 0; p < P; ++p) c += s_ids[p] < e;
+    s_off[e] = c;
+  }
+  __syncthreads();
+  for (int p = tid; p < P; p += nt) {
+    const int e = s_ids[p];
+    int pos = s_off[e];
+    for (int q = 0; q < p; ++q) pos += s_ids[q] == e;
+    s_sp[pos] = p;
+  }
+  __syncthreads();
+}
+
+template <int FMT, bool ROUTE>
 __global__ void __launch_bounds__(kSdThreads, 1)
-sd_ffn_kernel(FfnArgs a, SdLayout Ls, unsigned* bar_count, unsigned* bar_gen) {
+sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
   extern __shared__ uint8_t sd_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sd_raw) + 127) & ~uintptr_t(127));
   uint16_t* s_x = reinterpret_cast<uint16_t*>(sm + Ls.off_x);
-  float* s_red = reinterpret_cast<float*>(sm + Ls.off_red);   // [warp][m][16][8]
+  float* s_red = reinterpret_cast<float*>(sm + Ls.off_red);   // [buffer][warp][m][16][xrows]
   const int es = Ls.estride;
   int* s_a = reinterpret_cast<int*>(sm + Ls.off_rank);
   int* s_b = s_a + es;
@@ -329,26 +624,111 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, unsigned* bar_count, unsigned* bar_gen) {
   int* s_cnt = s_a + 3 * es;
   int* s_slot = s_a + 4 * es;
   float* s_ts = reinterpret_cast<float*>(s_a + 5 * es);   // [E][3]
-  int* s_tok = s_a + 8 * es;                               // token group: x row of each token
-  float* s_w = reinterpret_cast<float*>(s_a + 8 * es + 8); // and its combine weight
-  const uint32_t bars = smem_u32(sm + Ls.off_bar);              // full[4], empty[4]
-  int* s_flag = reinterpret_cast<int*>(sm + Ls.off_bar + 128);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + Ls.off_bar + 132);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* s_tok = s_a + 8 * es;                               // token group: token of each row
+  float* s_w = reinterpret_cast<float*>(s_a + 8 * es + 8); // its combine weight
+  int* s_pair = s_a + 8 * es + 16;                         // its pair index
+  int* s_scan = s_a + 8 * es + 32;                         // [64] scan scratch
+  // fused router scratch
+  float* s_logit = reinterpret_cast<float*>(sm + Ls.off_route);
+  const int P = a.T * a.k;
+  int* s_ids = reinterpret_cast<int*>(s_logit + (ROUTE ? a.T * a.E : 0));
+  float* s_val = reinterpret_cast<float*>(s_ids + P);
+  float* s_wt = s_val + P;
+  int* s_res = reinterpret_cast<int*>(s_wt + P);
+  int* s_sp = s_res + P;
+  int* s_expect = s_sp + P;
+  int* s_off = s_expect + a.T;
+  const uint32_t bars = smem_u32(sm + Ls.off_bar);   // full[8] at 0, empty[8] at 64, router rows at 128
+  // reduction buffers: red_full[i] (16 consumer arrivals: partials in) at 136 + 8i,
+  // red_empty[i] (the epilogue warp's arrival: partials read) at 152 + 8i
+  const uint32_t red_full = bars + 136, red_empty = bars + 152;
+  volatile int* s_flag = reinterpret_cast<volatile int*>(sm + Ls.off_bar + 176);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + Ls.off_bar + 180);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = Ls.stages;
+  const int G = gridDim.x, b = blockIdx.x;
 
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bars + 8 * s, 1);
       mbar_init(bars + 64 + 8 * s, kSdCons);
     }
+    mbar_init(bars + 128, 1);
+    for (int i = 0; i < kSdRedBufs; ++i) {
+      mbar_init(red_full + 8 * i, kSdCons);
+      mbar_init(red_empty + 8 * i, 1);
+    }
+    *s_flag = 1;
     *s_abort = 0;
     mbar_fence_init();
   }
+  __syncthreads();
+  bool ok = true;
+  const int ne = ROUTE ? (a.E > b ? (a.E - b + G - 1) / G : 0) : 0;   // router rows of this CTA
+  if (ROUTE) {
+    // router rows are weights: their copy may start before the previous kernel has finished
+    if (tid == 0 && ne > 0) {
+      mbar_arrive_expect_tx(bars + 128, uint32_t(ne * a.d * 2));
+      for (int i = 0; i < ne; ++i)
+        bulk_load(smem_u32(sm + size_t(i) * a.d * 2), ra.wr + size_t(b + i * G) * a.d, uint32_t(a.d * 2), bars + 128);
+    }
+  }
   pdl_wait();
-  sd_items(a, Ls.xrows, s_a, s_b, s_lo, s_cnt, s_slot, s_ts);   // all threads, ends with __syncthreads
+  if (ROUTE) {
+    // the slot table is read now, while the router step runs
+    if (a.slot_of)
+      for (int e = tid; e < a.E; e += kSdThreads) s_slot[e] = a.slot_of[e];
+    // this call's counters start at zero (the grid sync below orders this before any count)
+    const int nz = a.E + a.T * (a.d / 32);
+    for (int i = b * kSdThreads + tid; i < nz; i += G * kSdThreads) {
+      if (i < a.E) ra.ready[i] = 0u;
+      else ra.merge[i - a.E] = 0u;
+    }
+    if (warp >= 1 && warp <= kSdCons && ne > 0) {
+      if (mbar_wait_warp(bars + 128, 0, s_abort)) {
+        sd_route_logits(a, ra, sm, ne, warp - 1, lane);
+      } else {
+        *s_abort = 1;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      if (!grid_sync_mono(gsync, nullptr)) *s_abort = 1;
+    }
+    __syncthreads();
+    if (*s_abort) {
+      ok = false;
+      if (tid == 0) set_dev_err(DEV_ERR_GRID_TIMEOUT);
+    }
+    sd_route_select(a, ra, s_logit, s_ids, s_val, s_wt, s_sp, s_off);
+  }
+  // the pairs sorted by expert: this kernel's own (ROUTE) or the caller's
+  const int32_t* offsets = ROUTE ? s_off : a.offsets;
+  const int32_t* spair = ROUTE ? s_sp : a.sorted_pair;
+  // slot table: the copy taken during the router step (ROUTE) or the caller's
+  const int32_t* slot_src = ROUTE ? (a.slot_of ? s_slot : nullptr) : a.slot_of;
+  sd_items(a, offsets, slot_src, Ls.xrows, s_a, s_b, s_lo, s_cnt, s_slot, s_scan);   // all threads
+  if (ROUTE) {
+    for (int p = tid; p < P; p += kSdThreads) s_res[p] = s_slot[s_ids[p]] >= 0;
+    __syncthreads();
+    if (tid < a.T) {
+      int c = 0;
+      for (int q = 0; q < a.k; ++q) c += s_res[tid * a.k + q];
+      s_expect[tid] = c;
+    }
+    __syncthreads();
+    // a token without a resident expert gets zeros (no merge reaches it)
+    for (int t = b; t < a.T; t += G) {
+      if (s_expect[t] == 0) {
+        for (int c = tid; c < a.d; c += kSdThreads) {
+          ra.out_f32[size_t(t) * a.d + c] = 0.f;
+          if (ra.out_bf16) ra.out_bf16[size_t(t) * a.d + c] = 0;
+        }
+      }
+    }
+  }
   const int NA = s_a[a.E], NB = s_b[a.E];
-  const int G = gridDim.x, b = blockIdx.x;
   const int a_lo = int((long long)NA * b / G), a_hi = int((long long)NA * (b + 1) / G);
   const int b_lo = int((long long)NB * b / G), b_hi = int((long long)NB * (b + 1) / G);
   const int ua = a.f / kSdRowsA, ub = a.d / kSdRowsB;
@@ -358,42 +738,35 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, unsigned* bar_count, unsigned* bar_gen) {
   if (warp == 0) {
     // ---------------- producer ----------------
     uint32_t stage = 0, ph = 0;
-    bool ok = true;
-    for (int phase = 0; phase < 2 && ok; ++phase) {
+    bool pok = ok;
+    for (int phase = 0; phase < 2 && pok; ++phase) {
       const int i0 = phase ? b_lo : a_lo, i1 = phase ? b_hi : a_hi;
-      const int kc = phase ? Ls.kcB : Ls.kcA, nk = phase ? Ls.nkB : Ls.nkA;
-      const int cs = phase ? Ls.csB : Ls.csA, ss = phase ? Ls.ssB : Ls.ssA;
-      const int K = phase ? a.f : a.d, N = phase ? a.d : a.f;
-      const int nrows = phase ? kSdRowsB : 2 * kSdRowsA;
       const uint32_t bytes = uint32_t(phase ? blk_b : blk_a);
-      int ecur = -1;
-      for (int item = i0; item < i1 && ok; ++item) {
-        const SdItem it = sd_item(phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua, &ecur);
-        for (int kk = 0; kk < nk; ++kk) {
-          if (!mbar_wait(bars + 64 + 8 * stage, ph ^ 1, s_abort)) {
-            ok = false;
-            break;
-          }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(bars + 8 * stage, bytes);
-            const uint8_t* src = a.prep_dec + size_t(it.slot) * slot_bytes +
-                                 (phase ? size_t(a.f / kSdRowsA) * blk_a + size_t(it.n0) * blk_b
-                                        : size_t(it.n0) * blk_a);
-            bulk_load(smem_u32(sm + stage * Ls.stage_bytes), src, bytes, bars + 8 * stage);
-          }
-          __syncwarp();
-          if (++stage == uint32_t(S)) {
-            stage = 0;
-            ph ^= 1;
-          }
+      SdItem it;
+      for (int item = i0; item < i1 && pok; ++item) {
+        if (item == i0) sd_item_first(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua);
+        else sd_item_next(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, item, phase ? ub : ua);
+        if (!mbar_wait_warp(bars + 64 + 8 * stage, ph ^ 1, s_abort)) {
+          pok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bars + 8 * stage, bytes);
+          const uint8_t* src = a.prep_dec + size_t(it.slot) * slot_bytes +
+                               (phase ? size_t(a.f / kSdRowsA) * blk_a + size_t(it.n0) * blk_b
+                                      : size_t(it.n0) * blk_a);
+          bulk_load(smem_u32(sm + stage * Ls.stage_bytes), src, bytes, bars + 8 * stage);
+        }
+        __syncwarp();
+        if (++stage == uint32_t(S)) {
+          stage = 0;
+          ph ^= 1;
         }
       }
     }
-    if (!ok) {
-      if (lane == 0) {
-        set_dev_err(DEV_ERR_TIMEOUT);
-        *s_abort = 1;
-      }
+    if (!pok && ok && lane == 0) {
+      set_dev_err(DEV_ERR_TIMEOUT);
+      *s_abort = 1;
     }
     // let every copy issued land before the CTA can exit: wait for the last uses of each stage
     if (lane == 0) {
@@ -405,18 +778,174 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, unsigned* bar_count, unsigned* bar_gen) {
         --stage;
         mbar_wait(bars + 8 * stage, ph, nullptr);
       }
+      if (ROUTE && ne > 0 && !ok) mbar_wait(bars + 128, 0, nullptr);   // the router rows' copy
+    }
+    return;
+  }
+
+  const int xr = Ls.xrows;
+  uint16_t* h16 = reinterpret_cast<uint16_t*>(a.h);
+  if (warp == kSdEpiWarp) {
+    // ---------------- epilogue warp ----------------
+    // Per item, in the consumers' order: wait until the 16 partials are in, reduce them
+    // (in warp order), write h / y, free the buffer.  It meets the consumers at their
+    // named barriers, so the token group it reads is the current one.
+    sd_tensor_scales(a, s_a, s_slot, s_ts, lane, 32);
+    __syncwarp();
+    bool eok = ok;
+    int jred = 0;
+    unsigned pend_n = 0;   // finished gate/up items of the current expert not yet published
+    for (int phase = 0; phase < 2; ++phase) {
+      const int i0 = phase ? b_lo : a_lo, i1 = phase ? b_hi : a_hi;
+      if (!ROUTE && phase == 1) {
+        sd_work_sync();   // the consumers' grid sync happens between these
+        sd_work_sync();
+        if (!*s_flag) eok = false;
+      }
+      int staged_e = -1, staged_g = -1;
+      SdItem it;
+      for (int item = i0; item < i1; ++item) {
+        if (item == i0) sd_item_first(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua);
+        else sd_item_next(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, item, phase ? ub : ua);
+        const int p0 = it.grp * xr, n = min(xr, it.cnt - p0);
+        if (it.e != staged_e || it.grp != staged_g) {
+          sd_work_sync();   // (consumers restage the tokens between the two)
+          sd_work_sync();
+          if (!*s_flag) eok = false;
+          staged_e = it.e;
+          staged_g = it.grp;
+        }
+        const int buf = jred % Ls.nbufs, use = jred / Ls.nbufs;
+        ++jred;
+        if (eok && !mbar_wait_warp(red_full + 8 * buf, use & 1, s_abort)) {
+          eok = false;
+          *s_abort = 1;
+        }
+        if (!eok) continue;
+        const float* rb = s_red + buf * Ls.nred;
+        if (phase == 0) {
+          // h = silu(gate) * up for the item's 16 rows and n tokens, stored as f16.  Lane: row
+          // lane & 15, tokens (lane >> 4) + 2q.
+          float gs[4], us[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int row = lane & 15, tok = (lane >> 4) + 2 * q;
+            gs[q] = us[q] = 0.f;
+            if (tok < n) {
+#pragma unroll 4
+              for (int w = 0; w < kSdCons; ++w) {
+                gs[q] += rb[((w * 2 + 0) * 16 + row) * xr + tok];
+                us[q] += rb[((w * 2 + 1) * 16 + row) * xr + tok];
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(red_empty + 8 * buf);   // the buffer is free again
+          const float tsg = s_ts[3 * it.e + 0], tsu = s_ts[3 * it.e + 1];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int row = lane & 15, tok = (lane >> 4) + 2 * q;
+            if (tok < n) {
+              const float gg = gs[q] * tsg, uu = us[q] * tsu;
+              const float h = __fdividef(gg, 1.f + __expf(-gg)) * uu;
+              if (!isfinite(h)) set_dev_err(DEV_ERR_NONFINITE);
+              h16[size_t(it.lo + p0 + tok) * a.f + it.n0 * kSdRowsA + row] = __half_as_ushort(__float2half_rn(h));
+            }
+          }
+          if (ROUTE) {
+            // publish the expert's finished items once, after its last item in this CTA
+            ++pend_n;
+            if (item + 1 == i1 || item + 1 >= s_a[it.e + 1]) {
+              __syncwarp();
+              if (lane == 0) {
+                __threadfence();
+                atomicAdd(ra.ready + it.e, pend_n);
+              }
+              pend_n = 0;
+            }
+          }
+        } else {
+          // y for the item's 32 columns (lane) and n tokens
+          float yv[8];
+          const int tile = lane >> 4, row = lane & 15;
+#pragma unroll
+          for (int tok = 0; tok < 8; ++tok) {
+            yv[tok] = 0.f;
+            if (tok < n) {
+#pragma unroll 4
+              for (int q = 0; q < kSdCons / 2; ++q) yv[tok] += rb[(((2 * q + tile) * 2) * 16 + row) * xr + tok];
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(red_empty + 8 * buf);   // the buffer is free again
+          const float tsd = s_ts[3 * it.e + 2];
+          const int gcol = it.n0 * kSdRowsB + lane;
+#pragma unroll
+          for (int tok = 0; tok < 8; ++tok) {
+            if (tok < n) {
+              const float y = yv[tok] * tsd;
+              if (!isfinite(y)) set_dev_err(DEV_ERR_NONFINITE);
+              if (ROUTE) {
+                ra.ybuf[size_t(s_pair[tok]) * a.d + gcol] = y;
+              } else if (a.topk_w) {
+                atomicAdd(a.y_or_out + size_t(s_tok[tok]) * a.d + gcol, s_w[tok] * y);
+              } else {
+                a.y_or_out[size_t(it.lo + p0 + tok) * a.d + gcol] = y;
+              }
+            }
+          }
+          if (ROUTE) {
+            // count this pair in on each of its tokens' 32-column blocks; the last one merges
+            __syncwarp();
+            int fin = 0;
+            if (lane < n) {
+              const int tk = s_tok[lane];
+              const unsigned old = atom_add_acq_rel(ra.merge + size_t(tk) * (a.d / 32) + it.n0, 1u);
+              fin = int(old) + 1 == s_expect[tk];
+            }
+            unsigned fm = __ballot_sync(0xFFFFFFFFu, fin);
+            if (fm) __threadfence();
+            while (fm) {
+              const int tok = __ffs(fm) - 1;
+              fm &= fm - 1;
+              const int tk = s_tok[tok];
+              float o = 0.f;
+              for (int q0 = 0; q0 < a.k; q0 += 8) {
+                float yq[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const int pr = tk * a.k + q0 + q;
+                  yq[q] = (q0 + q < a.k && s_res[pr]) ? __ldcg(ra.ybuf + size_t(pr) * a.d + gcol) : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const int pr = tk * a.k + q0 + q;
+                  if (q0 + q < a.k && s_res[pr]) o = fmaf(s_wt[pr], yq[q], o);
+                }
+              }
+              ra.out_f32[size_t(tk) * a.d + gcol] = o;
+              if (ra.out_bf16) ra.out_bf16[size_t(tk) * a.d + gcol] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+            }
+          }
+        }
+      }
+    }
+    if (!eok && ok) set_dev_err(DEV_ERR_TIMEOUT);
+    if (!ROUTE && a.out_bf16) {
+      sd_work_sync();
+      sd_work_sync();
     }
     return;
   }
 
   // ---------------- consumers ----------------
-  const int cw = warp - 1;                 // consumer warp 0..7
-  const int ct = threadIdx.x - 32;         // consumer thread 0..255
+  const int cw = warp - 1;                 // consumer warp 0..15
+  const int ct = tid - 32;                 // consumer thread 0..511
   const int g = lane >> 2, t = lane & 3;
   uint32_t stage = 0, ph = 0;
-  bool ok = true;
+  int jred = 0;                            // items done: picks the reduction buffer
 
-  if (a.out_bf16) {
+  if (!ROUTE && a.out_bf16) {
     float4* o = reinterpret_cast<float4*>(a.y_or_out);
     const long long n4 = (long long)a.T * a.d / 4;
     for (long long i = (long long)b * (kSdCons * 32) + ct; i < n4; i += (long long)G * kSdCons * 32)
@@ -425,105 +954,94 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, unsigned* bar_count, unsigned* bar_gen) {
 
   for (int phase = 0; phase < 2; ++phase) {
     const int i0 = phase ? b_lo : a_lo, i1 = phase ? b_hi : a_hi;
-    const int kc = phase ? Ls.kcB : Ls.kcA, nk = phase ? Ls.nkB : Ls.nkA;
-    const int cs = phase ? Ls.csB : Ls.csA, ss = phase ? Ls.ssB : Ls.ssA;
     const int K = phase ? a.f : a.d;
-    const int nrows = phase ? kSdRowsB : 2 * kSdRowsA;
     const int st_x = K + 8;                // staged token row stride (f16)
-    if (phase == 1) {
-      // every h of every CTA is written before any is read
-      sd_cons_sync();
+    if (!ROUTE && phase == 1) {
+      // every h of every CTA is written before any is read (the epilogue warp is done with phase A)
+      sd_work_sync();
       if (ct == 0) {
-        int okb = 1;
-        const unsigned gg = *reinterpret_cast<volatile unsigned*>(bar_gen);
         __threadfence();
-        if (atomicAdd(bar_count, 1u) == unsigned(G) - 1) {
-          *reinterpret_cast<volatile unsigned*>(bar_count) = 0u;
-          __threadfence();
-          atomicAdd(bar_gen, 1u);
-        } else {
-          const unsigned long long t0 = globaltimer_ns();
-          for (uint32_t it = 0; *reinterpret_cast<volatile unsigned*>(bar_gen) == gg; ++it) {
-            if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) {
-              okb = 0;
-              set_dev_err(DEV_ERR_GRID_TIMEOUT);
-              break;
-            }
-            __nanosleep(64);
-          }
+        if (!grid_sync_mono(gsync, s_abort)) {
+          *s_flag = 0;
+          set_dev_err(DEV_ERR_GRID_TIMEOUT);
         }
-        __threadfence();
-        *s_flag = okb;
       }
-      sd_cons_sync();
+      sd_work_sync();
       if (!*s_flag) {
         ok = false;
         *s_abort = 1;
       }
     }
-    // On a failed wait `ok` turns false and the loops keep their shape (every consumer
-    // warp still reaches every barrier), skipping work, so no warp is left waiting.
-    int staged_e = -1, staged_g = -1, ecur = -1;
+    // On a failed wait `ok` turns false and the loops keep their shape (every warp still
+    // reaches every named barrier), skipping work, so no warp is left waiting.
+    int staged_e = -1, staged_g = -1;
+    // warp's share: phase A: both matrices, K sixteenth cw; phase B: row tile cw & 1, K eighth cw >> 1
+    const int nsb = K / 64;
+    const int parts = phase ? kSdCons / 2 : kSdCons;
+    const int kp = phase ? (cw >> 1) : cw;
+    const int sb_lo = kp * nsb / parts, sb_hi = (kp + 1) * nsb / parts;
+    SdItem it;
     for (int item = i0; item < i1; ++item) {
-      const SdItem it = sd_item(phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua, &ecur);
-      const int p0 = it.grp * Ls.xrows, n = min(Ls.xrows, it.cnt - p0);
+      if (item == i0) sd_item_first(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua);
+      else sd_item_next(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, item, phase ? ub : ua);
+      const int p0 = it.grp * xr, n = min(xr, it.cnt - p0);
       if (it.e != staged_e || it.grp != staged_g) {
-        sd_cons_sync();   // every warp is done with the previous tokens
+        if (ROUTE && phase == 1 && ct == 0 && ok) {
+          // the expert's h is complete once all of its gate/up items have counted in
+          if (!wait_count(ra.ready + it.e, unsigned(s_a[it.e + 1] - s_a[it.e]), s_abort)) {
+            *s_flag = 0;
+            set_dev_err(DEV_ERR_GRID_TIMEOUT);
+          }
+        }
+        sd_work_sync();   // every warp is done with the previous tokens (and their epilogues)
+        if (!*s_flag) {
+          ok = false;
+          *s_abort = 1;
+        }
         if (ct < n) {
-          const int p = a.sorted_pair[it.lo + p0 + ct];
+          const int p = spair[it.lo + p0 + ct];
+          s_pair[ct] = p;
           s_tok[ct] = p / a.k;
           s_w[ct] = a.topk_w ? a.topk_w[p] : 0.f;
         }
-        if (phase == 0) {
+        if (ok) {
           const int per = K / 8;
-          for (int c = ct; c < n * per; c += kSdCons * 32) {
-            const int q = c / per, cc = c % per;
-            const uint16_t* row = a.x + size_t(a.sorted_pair[it.lo + p0 + q] / a.k) * a.d;
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + cc);
-            uint4 hh;
-            hh.x = f16x2_of(bf16_lo(v.x), bf16_hi(v.x));
-            hh.y = f16x2_of(bf16_lo(v.y), bf16_hi(v.y));
-            hh.z = f16x2_of(bf16_lo(v.z), bf16_hi(v.z));
-            hh.w = f16x2_of(bf16_lo(v.w), bf16_hi(v.w));
-            *reinterpret_cast<uint4*>(s_x + q * st_x + 8 * cc) = hh;
-          }
-        } else {
-          const int per = K / 8;
-          for (int c = ct; c < n * per; c += kSdCons * 32) {
-            const int q = c / per, cc = c % per;
-            const float4* row = reinterpret_cast<const float4*>(a.h + size_t(it.lo + p0 + q) * a.f) + 2 * cc;
-            const float4 v0 = __ldcg(row), v1 = __ldcg(row + 1);
-            uint4 hh;
-            hh.x = f16x2_of(v0.x, v0.y);
-            hh.y = f16x2_of(v0.z, v0.w);
-            hh.z = f16x2_of(v1.x, v1.y);
-            hh.w = f16x2_of(v1.z, v1.w);
-            *reinterpret_cast<uint4*>(s_x + q * st_x + 8 * cc) = hh;
+          if (phase == 0) {
+            for (int c = ct; c < n * per; c += kSdCons * 32) {
+              const int q = c / per, cc = c % per;
+              const uint16_t* row = a.x + size_t(spair[it.lo + p0 + q] / a.k) * a.d;
+              const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + cc);
+              uint4 hh;
+              hh.x = f16x2_of(bf16_lo(v.x), bf16_hi(v.x));
+              hh.y = f16x2_of(bf16_lo(v.y), bf16_hi(v.y));
+              hh.z = f16x2_of(bf16_lo(v.z), bf16_hi(v.z));
+              hh.w = f16x2_of(bf16_lo(v.w), bf16_hi(v.w));
+              *reinterpret_cast<uint4*>(s_x + q * st_x + 8 * cc) = hh;
+            }
+          } else {
+            for (int c = ct; c < n * per; c += kSdCons * 32) {
+              const int q = c / per, cc = c % per;
+              const uint4 v = __ldcg(reinterpret_cast<const uint4*>(h16 + size_t(it.lo + p0 + q) * a.f) + cc);
+              *reinterpret_cast<uint4*>(s_x + q * st_x + 8 * cc) = v;
+            }
           }
         }
         staged_e = it.e;
         staged_g = it.grp;
-        sd_cons_sync();
+        sd_work_sync();
       }
-      // warp's share: phase A: both matrices, K eighth cw; phase B: row tile cw & 1, K quarter cw >> 1
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      const int nsb = kc / 64;
-      const int parts = phase ? kSdCons / 2 : kSdCons;
-      const int kp = phase ? (cw >> 1) : cw;
-      const int sb_lo = kp * nsb / parts, sb_hi = (kp + 1) * nsb / parts;
-      for (int kk = 0; kk < nk; ++kk) {
-        if (ok && !mbar_wait(bars + 8 * stage, ph, s_abort)) {
-          ok = false;
-          *s_abort = 1;
-        }
+      if (ok && !mbar_wait_warp(bars + 8 * stage, ph, s_abort)) {
+        ok = false;
+        *s_abort = 1;
+      }
+      if (ok) {
         const uint8_t* base = sm + stage * Ls.stage_bytes;
         // MMA token column g: rows past the staged ones read the last staged row (results unused)
-        const uint16_t* xrow = s_x + min(g, Ls.xrows - 1) * st_x + kk * kc + 16 * t;
-        if (!ok) {
-          // skip the work; the stage is still released below
-        } else if (phase == 0) {
+        const uint16_t* xrow = s_x + min(g, xr - 1) * st_x + 16 * t;
+        if (phase == 0) {
           // [gate codes][up codes][gate scales][up scales], 16 rows each
-          const int cb = kSdRowsA * (a.d / 2), sbb = kSdRowsA * ss;
+          const int cb = kSdRowsA * (a.d / 2), sbb = kSdRowsA * (a.d / (FMT == FTMOE_NVFP4 ? 16 : 32));
           const uint8_t* const cbase[2] = {base, base + cb};
           const uint8_t* const sbase[2] = {base + 2 * cb, base + 2 * cb + sbb};
           sd_tiles_mma<FMT, 2>(cbase, sbase, kSdRowsA, g, xrow, sb_lo, sb_hi, t, acc);
@@ -535,89 +1053,50 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, unsigned* bar_count, unsigned* bar_gen) {
           float (&acc1)[1][4] = *reinterpret_cast<float(*)[1][4]>(&acc[0]);
           sd_tiles_mma<FMT, 1>(cbase, sbase, kSdRowsB, tile * 16 + g, xrow, sb_lo, sb_hi, t, acc1);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 64 + 8 * stage);
-        if (++stage == uint32_t(S)) {
-          stage = 0;
-          ph ^= 1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 64 + 8 * stage);
+      if (++stage == uint32_t(S)) {
+        stage = 0;
+        ph ^= 1;
+      }
+      // ---- partials -> reduction buffer; the epilogue warp takes it from there ----
+      const int buf = jred % Ls.nbufs, use = jred / Ls.nbufs;
+      ++jred;
+      float* rb = s_red + buf * Ls.nred;
+      if (ok && !mbar_wait_warp(red_empty + 8 * buf, (use & 1) ^ 1, s_abort)) {
+        ok = false;
+        *s_abort = 1;
+      }
+      if (!ok) continue;
+      const int nm = phase ? 1 : 2;
+      for (int m = 0; m < nm; ++m) {
+        float* my = rb + ((cw * 2 + m) * 16) * xr;
+        if (2 * t < xr) {
+          my[g * xr + 2 * t] = acc[m][0];
+          my[(g + 8) * xr + 2 * t] = acc[m][2];
+        }
+        if (2 * t + 1 < xr) {
+          my[g * xr + 2 * t + 1] = acc[m][1];
+          my[(g + 8) * xr + 2 * t + 1] = acc[m][3];
         }
       }
-      // partials -> shared memory: [warp][m][row 16][token 8]
-      float* my = s_red + cw * 2 * 128;
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        my[m * 128 + g * 8 + 2 * t] = acc[m][0];
-        my[m * 128 + g * 8 + 2 * t + 1] = acc[m][1];
-        my[m * 128 + (g + 8) * 8 + 2 * t] = acc[m][2];
-        my[m * 128 + (g + 8) * 8 + 2 * t + 1] = acc[m][3];
-      }
-      sd_cons_sync();
-      if (!ok) {
-        // nothing to write
-      } else if (phase == 0) {
-        if (ct < 128) {
-          const int row = ct & 15, tok = ct >> 4;
-          if (tok < n) {
-            float gs = 0.f, us = 0.f;
-#pragma unroll
-            for (int w = 0; w < kSdCons; ++w) {
-              gs += s_red[w * 256 + row * 8 + tok];
-              us += s_red[w * 256 + 128 + row * 8 + tok];
-            }
-            const float tsg = s_ts[3 * it.e + 0], tsu = s_ts[3 * it.e + 1];
-            const float gg = gs * tsg, uu = us * tsu;
-            const float h = gg / (1.f + expf(-gg)) * uu;
-            if (!isfinite(h)) set_dev_err(DEV_ERR_NONFINITE);
-            a.h[size_t(it.lo + p0 + tok) * a.f + it.n0 * kSdRowsA + row] = h;
-          }
-        }
-      } else {
-        const int tile = (ct >> 7) & 1, row = ct & 15, tok = (ct >> 4) & 7;
-        if (ct < 256 && tok < n) {
-          float y = 0.f;
-#pragma unroll
-          for (int q = 0; q < kSdCons / 2; ++q) y += s_red[(2 * q + tile) * 256 + row * 8 + tok];
-          y *= s_ts[3 * it.e + 2];
-          if (!isfinite(y)) set_dev_err(DEV_ERR_NONFINITE);
-          const int i = p0 + tok;
-          const int col = it.n0 * kSdRowsB + tile * 16 + row;
-          if (a.topk_w) {
-            atomicAdd(a.y_or_out + size_t(s_tok[tok]) * a.d + col, s_w[tok] * y);
-          } else {
-            a.y_or_out[size_t(it.lo + i) * a.d + col] = y;
-          }
-        }
-      }
-      sd_cons_sync();   // s_red is free again
+      __syncwarp();
+      if (lane == 0) mbar_arrive(red_full + 8 * buf);
     }
   }
   if (!ok) set_dev_err(DEV_ERR_TIMEOUT);
-  if (a.out_bf16) {
+  if (!ROUTE && a.out_bf16) {
     // every add of every CTA has landed: cast out to bf16
-    sd_cons_sync();
+    sd_work_sync();
     if (ct == 0) {
-      int okb = 1;
-      const unsigned gg = *reinterpret_cast<volatile unsigned*>(bar_gen);
       __threadfence();
-      if (atomicAdd(bar_count, 1u) == unsigned(G) - 1) {
-        *reinterpret_cast<volatile unsigned*>(bar_count) = 0u;
-        __threadfence();
-        atomicAdd(bar_gen, 1u);
-      } else {
-        const unsigned long long t0 = globaltimer_ns();
-        for (uint32_t it = 0; *reinterpret_cast<volatile unsigned*>(bar_gen) == gg; ++it) {
-          if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) {
-            okb = 0;
-            set_dev_err(DEV_ERR_GRID_TIMEOUT);
-            break;
-          }
-          __nanosleep(64);
-        }
+      if (!grid_sync_mono(gsync, s_abort)) {
+        *s_flag = 0;
+        set_dev_err(DEV_ERR_GRID_TIMEOUT);
       }
-      __threadfence();
-      *s_flag = okb;
     }
-    sd_cons_sync();
+    sd_work_sync();
     if (!*s_flag || !ok) return;
     const float4* o = reinterpret_cast<const float4*>(a.y_or_out);
     uint2* ob = reinterpret_cast<uint2*>(a.out_bf16);

@@ -312,13 +312,14 @@ ftmoe_status ffn_dec_launch(const FfnArgs& a, int P, void* hdr, cudaStream_t st)
   unsigned* cnt = reinterpret_cast<unsigned*>(static_cast<char*>(hdr) + kWsBarrierCount);
   unsigned* gen = reinterpret_cast<unsigned*>(static_cast<char*>(hdr) + kWsBarrierGen);
   const int ms = max_smem_optin();
-  const int xrows = std::min(8, a.T);
-  if (a.prep_dec && sd_supported(a.E, a.d, a.f, FMT, xrows, ms)) {
+  if (a.prep_dec && sd_supported(a.E, a.d, a.f, FMT, a.T, a.k, ms)) {
     // streaming form: one CTA per SM, bulk copies into a shared-memory ring
-    const SdLayout Ls = sd_layout(a.E, a.d, a.f, FMT, xrows, ms);
-    const int per_sm = resident_ctas(sd_ffn_kernel<FMT>, kSdThreads, size_t(Ls.smem));
+    const SdLayout Ls = sd_layout(a.E, a.d, a.f, FMT, a.T, a.k, false, ms);
+    const int per_sm = resident_ctas(sd_ffn_kernel<FMT, false>, kSdThreads, size_t(Ls.smem));
     if (per_sm < 1) return FTMOE_ERR_CUDA;
-    return launch(sd_ffn_kernel<FMT>, dim3(num_sms()), dim3(kSdThreads), size_t(Ls.smem), st, a, Ls, cnt, gen);
+    unsigned long long* gs = reinterpret_cast<unsigned long long*>(static_cast<char*>(hdr) + kWsGridSync);
+    return launch(sd_ffn_kernel<FMT, false>, dim3(num_sms()), dim3(kSdThreads), size_t(Ls.smem), st, a, Ls, SdRoute{},
+                  gs);
   }
   const size_t smem = dec_smem_bytes(std::max(a.d, a.f));
   const int per_sm = resident_ctas(dec_ffn_kernel<FMT>, kDecWarps * 32, smem);
@@ -517,9 +518,9 @@ ftmoe_status ffn_tc8_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, con
   return launch_gemm8<1>(tA2, tD, tD, g, mts * (d->d / 256), st);
 }
 
-ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of, const uint16_t* x,
+FfnArgs make_ffn_args(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of, const uint16_t* x,
                       int T, const int32_t* off, const int32_t* sp, const float* topk_w, float* y_or_out, void* ws,
-                      void* hdr, cudaStream_t st, uint16_t* out_bf16 = nullptr) {
+                      uint16_t* out_bf16) {
   FfnArgs a;
   a.E = d->E;
   a.k = d->k;
@@ -545,6 +546,13 @@ ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const i
   a.prep_dec = (w->prepared && prep_decode_bytes(d, w->C))
                    ? static_cast<const uint8_t*>(w->prepared) + prep_decode_offset(d, w->C)
                    : nullptr;
+  return a;
+}
+
+ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of, const uint16_t* x,
+                      int T, const int32_t* off, const int32_t* sp, const float* topk_w, float* y_or_out, void* ws,
+                      void* hdr, cudaStream_t st, uint16_t* out_bf16 = nullptr) {
+  const FfnArgs a = make_ffn_args(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, out_bf16);
   const int P = T * d->k;
   if (ffn_path(d, T) == 1) return ffn_tc_impl(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, nullptr, st);
   if (ffn_path(d, T) == 2) return ffn_tc8_impl(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, nullptr, st);
@@ -793,7 +801,37 @@ ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* h, const int32_t* trace, int steps
 
 // --- whole layer -------------------------------------------------------------
 // Workspace: header | ids | w | offsets | sorted_pair | pair_pos | y | (route/permute/ffn scratch, shared)
+}  // extern "C"
+
 namespace {
+// Fused decode layer (router, expert FFN and merge in one kernel): few tokens, a 4-bit
+// format with the prepared decode layout.  Its scratch: h (f16) | logits | ready | merge.
+struct FusedWs {
+  size_t h, logits, ready, merge, total;
+};
+FusedWs fused_ws(const ftmoe_layer_desc* d, int T) {
+  FusedWs F;
+  const size_t P = size_t(T) * d->k;
+  size_t o = 0;
+  F.h = o; o += align256(P * d->ffn * 2);
+  F.logits = o; o += align256(size_t(T) * d->E * 4);
+  F.ready = o; o += align256(size_t(d->E) * 4);
+  F.merge = o; o += align256(size_t(T) * (d->d / 32) * 4);
+  F.total = o;
+  return F;
+}
+bool layer_fused_ok(const ftmoe_layer_desc* d, const ftmoe_weights* w, int T) {
+  if (ffn_path(d, T) != 0 || !w->prepared || !prep_decode_bytes(d, w->C)) return false;
+  return sd_route_supported(d->E, d->d, d->ffn, d->fmt, T, d->k, num_sms(), max_smem_optin());
+}
+template <int FMT>
+ftmoe_status layer_fused_launch(const FfnArgs& a, const SdRoute& r, void* hdr, cudaStream_t st) {
+  const SdLayout Ls = sd_layout(a.E, a.d, a.f, FMT, a.T, a.k, true, max_smem_optin());
+  if (resident_ctas(sd_ffn_kernel<FMT, true>, kSdThreads, size_t(Ls.smem)) < 1) return FTMOE_ERR_CUDA;
+  unsigned long long* gs = reinterpret_cast<unsigned long long*>(static_cast<char*>(hdr) + kWsGridSync);
+  return launch(sd_ffn_kernel<FMT, true>, dim3(num_sms()), dim3(kSdThreads), size_t(Ls.smem), st, a, Ls, r, gs);
+}
+
 struct LayerWs {
   size_t ids, w, off, sp, pp, y, scratch, total;
 };
@@ -813,15 +851,22 @@ LayerWs layer_ws(const ftmoe_layer_desc* d, int T) {
   const size_t sr = route_ws(d, T, true) - kWsHeader;
   const size_t sq = permute_ws(d, T) - kWsHeader;
   const size_t sf = ffn_ws(d, T) - kWsHeader;
-  o += std::max(sr, std::max(sq, sf));
+  o += std::max(std::max(sr, sq), std::max(sf, fused_ws(d, T).total));
   L.total = o;
   return L;
 }
 }  // namespace
 
+extern "C" {
+
 size_t ftmoe_layer_workspace_size(const ftmoe_layer_desc* d, int T) {
   if (!desc_ok(d) || T < 1) return 0;
   return layer_ws(d, T).total;
+}
+
+int ftmoe_layer_path(const ftmoe_layer_desc* d, const ftmoe_weights* w, int T) {
+  if (!desc_ok(d) || T < 1 || T > kMaxT || !weights_ok(d, w)) return -1;
+  return layer_fused_ok(d, w, T) ? 1 : 0;
 }
 
 ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of,
@@ -848,6 +893,27 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
   // ws + kWsHeader, so it gets a view that ends its header where scratch starts.
   char* view = base + L.scratch - kWsHeader;
   ftmoe_status s;
+  if (layer_fused_ok(d, w, T)) {
+    // one kernel: router + sort + expert FFN + merge
+    const FusedWs F = fused_ws(d, T);
+    char* sc = base + L.scratch;
+    FfnArgs a = make_ffn_args(d, w, slot_of, x, T, nullptr, nullptr, nullptr, out_f32, view, nullptr);
+    a.h = reinterpret_cast<float*>(sc + F.h);
+    SdRoute r;
+    r.wr = wr;
+    r.bias = bias;
+    r.renorm = d->renorm;
+    r.logits = reinterpret_cast<float*>(sc + F.logits);
+    r.ids = ids_;
+    r.tw = w_;
+    r.ready = reinterpret_cast<unsigned*>(sc + F.ready);
+    r.merge = reinterpret_cast<unsigned*>(sc + F.merge);
+    r.ybuf = y;
+    r.out_f32 = out_f32;
+    r.out_bf16 = out_bf16;
+    return d->fmt == FTMOE_NVFP4 ? layer_fused_launch<FTMOE_NVFP4>(a, r, base, st)
+                                 : layer_fused_launch<FTMOE_MXFP4>(a, r, base, st);
+  }
   // route: logits go to the scratch region (the view's buffer area)
   s = route_impl(d, x, wr, bias, T, ids_, w_, reinterpret_cast<float*>(base + L.scratch), base, st, off, sp, pp);
   if (s != FTMOE_OK) return s;

@@ -63,6 +63,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// The same wait for a whole warp: one lane polls, then every lane checks the completed
+// phase once (its own acquire of it).  Few threads polling the barrier word leave the
+// shared-memory pipe to the copies that complete it.  Warp-uniform result.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;   // usually complete already
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort);
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  if (ok) (void)mbar_try_wait(bar, parity);
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------------------
 // TMA: 2D tiled load and 1D bulk load into shared memory, completing on an mbarrier
 // ---------------------------------------------------------------------------

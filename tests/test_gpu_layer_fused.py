@@ -1,0 +1,175 @@
+"""ftmoe_layer_forward with few tokens and a 4-bit format runs router, sort, expert
+FFN and merge in one kernel.  Its results must equal, bit for bit, the separate
+calls (route -> permute -> expert_ffn -> combine), whose arithmetic it repeats,
+and match the oracle within the layer's tolerance (5e-3 relative L2):
+  * ids bit-exact with the oracle, weights and outputs within tolerance;
+  * T = 1 .. 8, NVFP4 and MXFP4, bias and renorm;
+  * skipped experts (slot -1), including a token none of whose experts is
+    resident (its output row is zero);
+  * repeated calls on one workspace (the kernel's counters start at zero each call);
+  * the full decode layer shape (128 experts, top-8, d 2048, ffn 768).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import ffn as OF
+
+from gpu_helpers import combine, ensure_built, expert_ffn, permute, route
+from helpers import bf16_bits, rel_l2, weights_to_numpy
+import sparse_moe_expert_sorted_b300 as ft
+
+pytestmark = pytest.mark.gpu
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def _layer(dsc, W, slot, x, wr, bias, ws=None, want_bf16=True):
+    T = x.shape[0]
+    ids = torch.full((T, dsc.k), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((T, dsc.k), float("nan"), dtype=torch.float32, device="cuda")
+    of = torch.full((T, dsc.d), float("nan"), dtype=torch.float32, device="cuda")
+    ob = torch.empty(T, dsc.d, dtype=torch.bfloat16, device="cuda") if want_bf16 else None
+    if ws is None:
+        ws = ft.workspace(ft.layer_workspace_size(dsc, T))
+    ft.layer_forward(dsc, ft.weights_struct(W), slot, x, wr, bias, ids, w, of, ob, ws)
+    return ids, w, of, ob
+
+
+def _separate(dsc, W, slot, x, wr, bias):
+    T = x.shape[0]
+    ids, w, _ = route(dsc, x, wr, bias)
+    off, sp, pp = permute(dsc, ids)
+    y = expert_ffn(dsc, W, slot, x, off, sp)
+    of, ob = combine(dsc, T, y, pp, w, ids, slot)
+    return ids, w, of, ob
+
+
+CASES = [
+    # fmt, E, k, d, f, T, renorm, zipf
+    (synth.NVFP4, 16, 8, 512, 256, 1, 0, 0.0),
+    (synth.NVFP4, 16, 8, 512, 256, 3, 1, 1.1),
+    (synth.NVFP4, 24, 4, 256, 384, 8, 0, 1.1),
+    (synth.MXFP4, 32, 6, 512, 256, 1, 1, 1.0),
+    (synth.MXFP4, 32, 6, 256, 512, 5, 0, 0.0),
+    (synth.NVFP4, 300, 2, 256, 128, 2, 0, 0.0),   # more experts than SMs: two router rows per CTA
+]
+
+
+@pytest.mark.parametrize("fmt,E,k,d,f,T,renorm,zipf", CASES)
+def test_fused_layer_matches_separate_calls_and_oracle(fmt, E, k, d, f, T, renorm, zipf):
+    seed = 31 * T + E
+    W = synth.make_experts(fmt, E, d, f, seed, device="cuda")
+    x = synth.make_x(T, d, seed, device="cuda")
+    wr = synth.make_router(E, d, seed, device="cuda")
+    bias_np = synth.make_zipf_bias(E, zipf, seed) if zipf else None
+    bias = torch.from_numpy(bias_np).cuda() if zipf else None
+    dsc = ft.desc(E, k, d, f, fmt, renorm)
+    ft.prepare_weights(dsc, W)
+    slot_np = ((np.arange(E) * 7 + 1) % E).astype(np.int32)
+    if np.gcd(7, E) != 1:
+        slot_np = np.arange(E, dtype=np.int32)[::-1].copy()
+    slot = torch.from_numpy(slot_np).cuda()
+    assert ft.layer_path(dsc, ft.weights_struct(W), T) == 1
+    ids, w, of, ob = _layer(dsc, W, slot, x, wr, bias)
+    ids_s, w_s, of_s, ob_s = _separate(dsc, W, slot, x, wr, bias)
+    assert torch.equal(ids, ids_s)
+    assert torch.equal(w, w_s)
+    assert torch.equal(of, of_s)
+    assert torch.equal(ob, ob_s)
+    ref = OF.layer(weights_to_numpy(W.to("cpu")), slot_np, bf16_bits(x.cpu()), bf16_bits(wr.cpu()), bias_np, k,
+                   renorm)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert rel_l2(w.cpu().numpy(), ref["w"]) < 1e-5
+    assert rel_l2(of.cpu().numpy(), ref["out"]) < TOL
+    assert rel_l2(ob.float().cpu().numpy(), ref["out"]) < TOL
+    assert ft.get_device_error() == 0
+
+
+def test_skipped_experts_and_a_token_with_none_resident():
+    fmt, E, k, d, f, T = synth.NVFP4, 16, 2, 256, 256, 4
+    W = synth.make_experts(fmt, E, d, f, 5, device="cuda")
+    x = synth.make_x(T, d, 5, device="cuda")
+    wr = synth.make_router(E, d, 5, device="cuda")
+    dsc = ft.desc(E, k, d, f, fmt)
+    ft.prepare_weights(dsc, W)
+    ref_full = OF.layer(weights_to_numpy(W.to("cpu")), np.arange(E, dtype=np.int32), bf16_bits(x.cpu()),
+                        bf16_bits(wr.cpu()), None, k, 1)
+    ids0 = ref_full["ids"]
+    # token 0 loses both of its experts; every other expert stays resident unless token 0 uses it
+    slot_np = np.arange(E, dtype=np.int32)
+    slot_np[ids0[0]] = -1
+    slot = torch.from_numpy(slot_np).cuda()
+    ids, w, of, ob = _layer(dsc, W, slot, x, wr, None)
+    ref = OF.layer(weights_to_numpy(W.to("cpu")), slot_np, bf16_bits(x.cpu()), bf16_bits(wr.cpu()), None, k, 1)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert torch.count_nonzero(of[0]).item() == 0
+    assert torch.count_nonzero(ob[0].float()).item() == 0
+    assert rel_l2(of.cpu().numpy(), ref["out"]) < TOL
+    _, _, of_s, _ = _separate(dsc, W, slot, x, wr, None)
+    assert torch.equal(of, of_s)
+    # the two halves of an exact split merge to the full output
+    slot_b = np.where(slot_np < 0, np.arange(E), -1).astype(np.int32)
+    _, _, of_b, _ = _layer(dsc, W, torch.from_numpy(slot_b).cuda(), x, wr, None)
+    _, _, of_full, _ = _layer(dsc, W, torch.arange(E, dtype=torch.int32, device="cuda"), x, wr, None)
+    assert rel_l2((of + of_b).cpu().numpy(), of_full.cpu().numpy()) < 1e-6
+    assert ft.get_device_error() == 0
+
+
+def test_repeated_calls_share_one_workspace():
+    fmt, E, k, d, f = synth.NVFP4, 32, 4, 512, 256
+    W = synth.make_experts(fmt, E, d, f, 8, device="cuda")
+    wr = synth.make_router(E, d, 8, device="cuda")
+    dsc = ft.desc(E, k, d, f, fmt)
+    ft.prepare_weights(dsc, W)
+    slot = torch.arange(E, dtype=torch.int32, device="cuda")
+    for T in (2, 7):
+        ws = ft.workspace(ft.layer_workspace_size(dsc, T))
+        outs = []
+        for rep in range(4):
+            x = synth.make_x(T, d, 100 + rep, device="cuda")
+            ids, w, of, ob = _layer(dsc, W, slot, x, wr, None, ws=ws, want_bf16=(rep % 2 == 0))
+            _, _, of_s, _ = _separate(dsc, W, slot, x, wr, None)
+            assert torch.equal(of, of_s)
+            outs.append(of)
+        assert not torch.equal(outs[0], outs[1])
+    assert ft.get_device_error() == 0
+
+
+def test_full_decode_layer_shape():
+    L = synth.DECODE.layer
+    dsc = ft.desc(L.E, L.k, L.d, L.f, L.fmt, L.renorm)
+    W = synth.make_experts(L.fmt, L.E, L.d, L.f, 11, device="cuda")
+    ft.prepare_weights(dsc, W)
+    wr = synth.make_router(L.E, L.d, 11, device="cuda")
+    bias_np = synth.make_zipf_bias(L.E, synth.DECODE.zipf_s, 11)
+    bias = torch.from_numpy(bias_np).cuda()
+    slot = torch.arange(L.E, dtype=torch.int32, device="cuda")
+    for T in (1, 4):
+        assert ft.layer_path(dsc, ft.weights_struct(W), T) == 1
+        x = synth.make_x(T, L.d, 12 + T, device="cuda")
+        ids, w, of, ob = _layer(dsc, W, slot, x, wr, bias)
+        _, _, of_s, ob_s = _separate(dsc, W, slot, x, wr, bias)
+        assert torch.equal(of, of_s) and torch.equal(ob, ob_s)
+        ref = OF.layer(weights_to_numpy(W.to("cpu")), np.arange(L.E, dtype=np.int32), bf16_bits(x.cpu()),
+                       bf16_bits(wr.cpu()), bias_np, L.k, L.renorm)
+        assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+        assert rel_l2(of.cpu().numpy(), ref["out"]) < TOL
+    assert ft.get_device_error() == 0
+
+
+def test_layer_path_query():
+    L = synth.DECODE.layer
+    dsc = ft.desc(L.E, L.k, L.d, L.f, L.fmt, L.renorm)
+    W = synth.make_experts(L.fmt, 4, L.d, L.f, 1, device="cuda")
+    assert ft.layer_path(dsc, ft.weights_struct(W), 1) == 0       # not prepared: separate steps
+    ft.prepare_weights(dsc, W)
+    assert ft.layer_path(dsc, ft.weights_struct(W), 1) == 1
+    assert ft.layer_path(dsc, ft.weights_struct(W), 8) == 1
+    assert ft.layer_path(dsc, ft.weights_struct(W), 9) == 0       # more tokens: separate steps
+    assert ft.layer_path(dsc, ft.weights_struct(W), 0) == -1
