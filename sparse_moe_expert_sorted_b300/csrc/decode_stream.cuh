@@ -326,22 +326,35 @@ __device__ __forceinline__ void sd_work_sync() { asm volatile("bar.sync 1, %0;" 
 // MMAs of NT 16-row tiles (NT = 2: gate and up, sharing the token fragments) over
 // super-blocks [sb_lo, sb_hi) of a staged tile.  Tile m: codes at cbase[m], scales at
 // sbase[m], in a prepared block of R rows; this lane's fragment rows are r and r + 8.
-template <int FMT, int NT>
+// Addresses advance by constant strides per super-block (R is a compile-time constant).
+template <int FMT, int NT, int R>
 __device__ __forceinline__ void sd_tiles_mma(const uint8_t* const (&cbase)[NT], const uint8_t* const (&sbase)[NT],
-                                             int R, int r, const uint16_t* xrow, int sb_lo, int sb_hi, int t,
+                                             int r, const uint16_t* xrow, int sb_lo, int sb_hi, int t,
                                              float (&acc)[NT][4]) {
-  const int half = (t & 1) * 8;
+  constexpr int kCodeStep = 32 * R;                               // bytes of codes per super-block
+  constexpr int kScaleStep = (FMT == FTMOE_NVFP4 ? 4 : 2) * R;    // bytes of scales per super-block
+  const uint8_t* pc[NT];
+  const uint8_t* ps[NT];
+#pragma unroll
+  for (int m = 0; m < NT; ++m) {
+    pc[m] = cbase[m] + ((t >> 1) * R + r) * 16 + (t & 1) * 8 + sb_lo * kCodeStep;
+    ps[m] = sbase[m] + (FMT == FTMOE_NVFP4 ? t : (t >> 1)) * R + r + sb_lo * kScaleStep;
+  }
+  const uint16_t* px = xrow + 64 * sb_lo;
   for (int sb0 = sb_lo; sb0 < sb_hi; sb0 += 8) {
     const int nc = min(8, sb_hi - sb0);
-    // MXFP4: rebase the chunk's scales on their maximum exponent
+    // MXFP4: rebase the chunk's scales on their maximum exponent.  The maximum runs over both
+    // 32-blocks of every super-block, so the four lanes of a row (whose products one MMA
+    // sums) share it.
     int e0[NT][2];
 #pragma unroll
     for (int m = 0; m < NT; ++m) {
       e0[m][0] = e0[m][1] = 0;
       if (FMT == FTMOE_MXFP4) {
-        for (int b = 2 * sb0; b < 2 * (sb0 + nc); ++b) {
-          e0[m][0] = max(e0[m][0], int(sbase[m][b * R + r]));
-          e0[m][1] = max(e0[m][1], int(sbase[m][b * R + r + 8]));
+        const uint8_t* q = sbase[m] + r + sb0 * kScaleStep;
+        for (int bk = 0; bk < 2 * nc; ++bk) {
+          e0[m][0] = max(e0[m][0], int(q[bk * R]));
+          e0[m][1] = max(e0[m][1], int(q[bk * R + 8]));
         }
       }
     }
@@ -352,24 +365,24 @@ __device__ __forceinline__ void sd_tiles_mma(const uint8_t* const (&cbase)[NT], 
       for (int i = 0; i < 4; ++i) part[m][i] = 0.f;
 #pragma unroll 1
     for (int c = 0; c < nc; ++c) {
-      const int sb = sb0 + c;
-      const uint16_t* xp = xrow + 64 * sb;
-      const uint4 x0 = *reinterpret_cast<const uint4*>(xp);
-      const uint4 x1 = *reinterpret_cast<const uint4*>(xp + 8);
+      const uint4 x0 = *reinterpret_cast<const uint4*>(px);
+      const uint4 x1 = *reinterpret_cast<const uint4*>(px + 8);
+      px += 64;
       const uint32_t B[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      const int chunk = 2 * sb + (t >> 1);
 #pragma unroll
       for (int m = 0; m < NT; ++m) {
-        const uint2 ca = *reinterpret_cast<const uint2*>(cbase[m] + (chunk * R + r) * 16 + half);
-        const uint2 cb = *reinterpret_cast<const uint2*>(cbase[m] + (chunk * R + r + 8) * 16 + half);
+        const uint2 ca = *reinterpret_cast<const uint2*>(pc[m]);
+        const uint2 cb = *reinterpret_cast<const uint2*>(pc[m] + 128);
         uint32_t pre0, pre1;
         if (FMT == FTMOE_NVFP4) {
-          pre0 = e4m3_f16x2(sbase[m][(4 * sb + t) * R + r]);
-          pre1 = e4m3_f16x2(sbase[m][(4 * sb + t) * R + r + 8]);
+          pre0 = e4m3_f16x2(ps[m][0]);
+          pre1 = e4m3_f16x2(ps[m][8]);
         } else {
-          pre0 = pow2_f16x2(int(sbase[m][(2 * sb + (t >> 1)) * R + r]) - e0[m][0]);
-          pre1 = pow2_f16x2(int(sbase[m][(2 * sb + (t >> 1)) * R + r + 8]) - e0[m][1]);
+          pre0 = pow2_f16x2(int(ps[m][0]) - e0[m][0]);
+          pre1 = pow2_f16x2(int(ps[m][8]) - e0[m][1]);
         }
+        pc[m] += kCodeStep;
+        ps[m] += kScaleStep;
         // byte i of the lane's 8 code bytes -> fa[i] (row r), fb[i] (row r + 8)
         uint32_t fa[8], fb[8];
         e2m1x8_to_f16x8(ca.x, *reinterpret_cast<uint32_t(*)[4]>(fa));
@@ -815,7 +828,7 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
           staged_e = it.e;
           staged_g = it.grp;
         }
-        const int buf = jred % Ls.nbufs, use = jred / Ls.nbufs;
+        const int buf = jred & (Ls.nbufs - 1), use = jred >> (Ls.nbufs - 1);
         ++jred;
         if (eok && !mbar_wait_warp(red_full + 8 * buf, use & 1, s_abort)) {
           eok = false;
@@ -1044,14 +1057,14 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
           const int cb = kSdRowsA * (a.d / 2), sbb = kSdRowsA * (a.d / (FMT == FTMOE_NVFP4 ? 16 : 32));
           const uint8_t* const cbase[2] = {base, base + cb};
           const uint8_t* const sbase[2] = {base + 2 * cb, base + 2 * cb + sbb};
-          sd_tiles_mma<FMT, 2>(cbase, sbase, kSdRowsA, g, xrow, sb_lo, sb_hi, t, acc);
+          sd_tiles_mma<FMT, 2, kSdRowsA>(cbase, sbase, g, xrow, sb_lo, sb_hi, t, acc);
         } else {
           // [down codes][down scales], 32 rows; this warp's 16-row half
           const int tile = cw & 1;
           const uint8_t* const cbase[1] = {base};
           const uint8_t* const sbase[1] = {base + kSdRowsB * (a.f / 2)};
           float (&acc1)[1][4] = *reinterpret_cast<float(*)[1][4]>(&acc[0]);
-          sd_tiles_mma<FMT, 1>(cbase, sbase, kSdRowsB, tile * 16 + g, xrow, sb_lo, sb_hi, t, acc1);
+          sd_tiles_mma<FMT, 1, kSdRowsB>(cbase, sbase, tile * 16 + g, xrow, sb_lo, sb_hi, t, acc1);
         }
       }
       __syncwarp();
@@ -1061,7 +1074,7 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
         ph ^= 1;
       }
       // ---- partials -> reduction buffer; the epilogue warp takes it from there ----
-      const int buf = jred % Ls.nbufs, use = jred / Ls.nbufs;
+      const int buf = jred & (Ls.nbufs - 1), use = jred >> (Ls.nbufs - 1);
       ++jred;
       float* rb = s_red + buf * Ls.nred;
       if (ok && !mbar_wait_warp(red_empty + 8 * buf, (use & 1) ^ 1, s_abort)) {
