@@ -556,32 +556,28 @@ __device__ __forceinline__ void sd_route_select(const FfnArgs& a, const SdRoute&
   const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < T * E; i += nt) s_logit[i] = __ldcg(r.logits + i);
   __syncthreads();
-  // rank of (t, e) = experts that come before it; the first k ranks are the selection
-  for (int i = tid; i < T * E; i += nt) {
+  // rank of (t, e) = experts that come before it; the first k ranks are the selection.
+  // Four neighbouring threads share a (t, e) and split the comparisons four ways.
+  const int n4 = 4 * T * E, n4w = (n4 + 31) & ~31;   // whole warps take part in the shuffles
+  for (int i4 = tid; i4 < n4w; i4 += nt) {
+    const bool act = i4 < n4;
+    const int i = act ? i4 >> 2 : 0, part = i4 & 3;
     const int t = i / E, e = i - t * E;
     const float v = s_logit[i];
     const float* row = s_logit + t * E;
+    const int j0 = act ? part * E / 4 : 0, j1 = act ? (part + 1) * E / 4 : 0;
     int rank = 0;
     if (!isnan(v)) {
-      if ((E & 3) == 0 && ((t * E) & 3) == 0) {
-        const float4* r4 = reinterpret_cast<const float4*>(row);
-#pragma unroll 4
-        for (int j4 = 0; j4 < E / 4; ++j4) {
-          const float4 u = r4[j4];
-          const int j = 4 * j4;
-          rank += ((u.x > v) || (u.x == v && j < e)) + ((u.y > v) || (u.y == v && j + 1 < e)) +
-                  ((u.z > v) || (u.z == v && j + 2 < e)) + ((u.w > v) || (u.w == v && j + 3 < e));
-        }
-      } else {
-        for (int j = 0; j < E; ++j) {
-          const float u = row[j];
-          rank += (u > v) || (u == v && j < e);
-        }
+      for (int j = j0; j < j1; ++j) {
+        const float u = row[j];
+        rank += (u > v) || (u == v && j < e);
       }
     } else {
-      for (int j = 0; j < E; ++j) rank += !isnan(row[j]) || j < e;
+      for (int j = j0; j < j1; ++j) rank += !isnan(row[j]) || j < e;
     }
-    if (rank < k) {
+    rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 1);
+    rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 2);
+    if (act && part == 0 && rank < k) {
       s_ids[t * k + rank] = e;
       s_val[t * k + rank] = v;
     }
@@ -722,28 +718,10 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
   // slot table: the copy taken during the router step (ROUTE) or the caller's
   const int32_t* slot_src = ROUTE ? (a.slot_of ? s_slot : nullptr) : a.slot_of;
   sd_items(a, offsets, slot_src, Ls.xrows, s_a, s_b, s_lo, s_cnt, s_slot, s_scan);   // all threads
-  if (ROUTE) {
-    for (int p = tid; p < P; p += kSdThreads) s_res[p] = s_slot[s_ids[p]] >= 0;
-    __syncthreads();
-    if (tid < a.T) {
-      int c = 0;
-      for (int q = 0; q < a.k; ++q) c += s_res[tid * a.k + q];
-      s_expect[tid] = c;
-    }
-    __syncthreads();
-    // a token without a resident expert gets zeros (no merge reaches it)
-    for (int t = b; t < a.T; t += G) {
-      if (s_expect[t] == 0) {
-        for (int c = tid; c < a.d; c += kSdThreads) {
-          ra.out_f32[size_t(t) * a.d + c] = 0.f;
-          if (ra.out_bf16) ra.out_bf16[size_t(t) * a.d + c] = 0;
-        }
-      }
-    }
-  }
   const int NA = s_a[a.E], NB = s_b[a.E];
-  const int a_lo = int((long long)NA * b / G), a_hi = int((long long)NA * (b + 1) / G);
-  const int b_lo = int((long long)NB * b / G), b_hi = int((long long)NB * (b + 1) / G);
+  // item ranges of this CTA (32-bit: items * grid stays far below 2^32)
+  const int a_lo = int(unsigned(NA) * unsigned(b) / unsigned(G)), a_hi = int(unsigned(NA) * unsigned(b + 1) / unsigned(G));
+  const int b_lo = int(unsigned(NB) * unsigned(b) / unsigned(G)), b_hi = int(unsigned(NB) * unsigned(b + 1) / unsigned(G));
   const int ua = a.f / kSdRowsA, ub = a.d / kSdRowsB;
   const size_t blk_a = sd_block_bytes_a(a.d, FMT), blk_b = sd_block_bytes_b(a.f, FMT);
   const size_t slot_bytes = sd_slot_bytes(a.d, a.f, FMT);
@@ -804,6 +782,26 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
     // (in warp order), write h / y, free the buffer.  It meets the consumers at their
     // named barriers, so the token group it reads is the current one.
     sd_tensor_scales(a, s_a, s_slot, s_ts, lane, 32);
+    if (ROUTE) {
+      // which pairs are resident, how many merges each token expects; a token without a
+      // resident expert gets zeros (no merge reaches it).  Only this warp reads these.
+      for (int p = lane; p < P; p += 32) s_res[p] = s_slot[s_ids[p]] >= 0;
+      __syncwarp();
+      for (int tk = lane; tk < a.T; tk += 32) {
+        int c = 0;
+        for (int q = 0; q < a.k; ++q) c += s_res[tk * a.k + q];
+        s_expect[tk] = c;
+      }
+      __syncwarp();
+      for (int tk = b; tk < a.T; tk += G) {
+        if (s_expect[tk] == 0) {
+          for (int c = lane; c < a.d; c += 32) {
+            ra.out_f32[size_t(tk) * a.d + c] = 0.f;
+            if (ra.out_bf16) ra.out_bf16[size_t(tk) * a.d + c] = 0;
+          }
+        }
+      }
+    }
     __syncwarp();
     bool eok = ok;
     int jred = 0;
