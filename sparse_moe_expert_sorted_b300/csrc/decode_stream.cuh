@@ -721,8 +721,22 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
   const int NA = s_a[a.E], NB = s_b[a.E];
   // item ranges of this CTA (32-bit: items * grid stays far below 2^32)
   const int a_lo = int(unsigned(NA) * unsigned(b) / unsigned(G)), a_hi = int(unsigned(NA) * unsigned(b + 1) / unsigned(G));
-  const int b_lo = int(unsigned(NB) * unsigned(b) / unsigned(G)), b_hi = int(unsigned(NB) * unsigned(b + 1) / unsigned(G));
+  // one-token layer call: down ranges in reverse CTA order, so the CTAs that finish their (strided)
+  // gate/up items first take the experts whose gate/up items finished first
+  const int bb = (ROUTE && a.T == 1) ? G - 1 - b : b;
+  const int b_lo = int(unsigned(NB) * unsigned(bb) / unsigned(G)), b_hi = int(unsigned(NB) * unsigned(bb + 1) / unsigned(G));
   const int ua = a.f / kSdRowsA, ub = a.d / kSdRowsB;
+  // Item sequence of a phase: contiguous [lo, hi), except the gate/up items of a one-token layer
+  // call, which a CTA takes strided by the grid (b, b + G, ...).  With one token every expert
+  // shares the staged x, and the strided order finishes the first experts' gate/up items
+  // early, so their down items need not wait for the slowest CTA.
+  const bool strided_a = ROUTE && a.T == 1;
+  auto seq_first = [&](int phase) { return (phase == 0 && strided_a) ? b : (phase ? b_lo : a_lo); };
+  auto seq_step = [&](int phase) { return (phase == 0 && strided_a) ? G : 1; };
+  auto seq_count = [&](int phase) {
+    if (phase == 0 && strided_a) return NA > b ? (NA - b + G - 1) / G : 0;
+    return phase ? b_hi - b_lo : a_hi - a_lo;
+  };
   const size_t blk_a = sd_block_bytes_a(a.d, FMT), blk_b = sd_block_bytes_b(a.f, FMT);
   const size_t slot_bytes = sd_slot_bytes(a.d, a.f, FMT);
 
@@ -731,11 +745,12 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
     uint32_t stage = 0, ph = 0;
     bool pok = ok;
     for (int phase = 0; phase < 2 && pok; ++phase) {
-      const int i0 = phase ? b_lo : a_lo, i1 = phase ? b_hi : a_hi;
+      const int first = seq_first(phase), step = seq_step(phase), count = seq_count(phase);
       const uint32_t bytes = uint32_t(phase ? blk_b : blk_a);
       SdItem it;
-      for (int item = i0; item < i1 && pok; ++item) {
-        if (item == i0) sd_item_first(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua);
+      for (int q = 0; q < count && pok; ++q) {
+        const int item = first + q * step;
+        if (q == 0 || step != 1) sd_item_first(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua);
         else sd_item_next(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, item, phase ? ub : ua);
         if (!mbar_wait_warp(bars + 64 + 8 * stage, ph ^ 1, s_abort)) {
           pok = false;
@@ -807,7 +822,7 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
     int jred = 0;
     unsigned pend_n = 0;   // finished gate/up items of the current expert not yet published
     for (int phase = 0; phase < 2; ++phase) {
-      const int i0 = phase ? b_lo : a_lo, i1 = phase ? b_hi : a_hi;
+      const int first = seq_first(phase), step = seq_step(phase), count = seq_count(phase);
       if (!ROUTE && phase == 1) {
         sd_work_sync();   // the consumers' grid sync happens between these
         sd_work_sync();
@@ -815,11 +830,12 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
       }
       int staged_e = -1, staged_g = -1;
       SdItem it;
-      for (int item = i0; item < i1; ++item) {
-        if (item == i0) sd_item_first(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua);
+      for (int q = 0; q < count; ++q) {
+        const int item = first + q * step;
+        if (q == 0 || step != 1) sd_item_first(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua);
         else sd_item_next(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, item, phase ? ub : ua);
         const int p0 = it.grp * xr, n = min(xr, it.cnt - p0);
-        if (it.e != staged_e || it.grp != staged_g) {
+        if (step != 1 ? q == 0 : (it.e != staged_e || it.grp != staged_g)) {
           sd_work_sync();   // (consumers restage the tokens between the two)
           sd_work_sync();
           if (!*s_flag) eok = false;
@@ -866,7 +882,7 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
           if (ROUTE) {
             // publish the expert's finished items once, after its last item in this CTA
             ++pend_n;
-            if (item + 1 == i1 || item + 1 >= s_a[it.e + 1]) {
+            if (q + 1 == count || item + step >= s_a[it.e + 1]) {
               __syncwarp();
               if (lane == 0) {
                 __threadfence();
@@ -964,7 +980,7 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
   }
 
   for (int phase = 0; phase < 2; ++phase) {
-    const int i0 = phase ? b_lo : a_lo, i1 = phase ? b_hi : a_hi;
+    const int first = seq_first(phase), step = seq_step(phase), count = seq_count(phase);
     const int K = phase ? a.f : a.d;
     const int st_x = K + 8;                // staged token row stride (f16)
     if (!ROUTE && phase == 1) {
@@ -992,11 +1008,12 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
     const int kp = phase ? (cw >> 1) : cw;
     const int sb_lo = kp * nsb / parts, sb_hi = (kp + 1) * nsb / parts;
     SdItem it;
-    for (int item = i0; item < i1; ++item) {
-      if (item == i0) sd_item_first(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua);
+    for (int q = 0; q < count; ++q) {
+      const int item = first + q * step;
+      if (q == 0 || step != 1) sd_item_first(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, a.E, item, phase ? ub : ua);
       else sd_item_next(it, phase ? s_b : s_a, s_lo, s_cnt, s_slot, item, phase ? ub : ua);
       const int p0 = it.grp * xr, n = min(xr, it.cnt - p0);
-      if (it.e != staged_e || it.grp != staged_g) {
+      if (step != 1 ? q == 0 : (it.e != staged_e || it.grp != staged_g)) {
         if (ROUTE && phase == 1 && ct == 0 && ok) {
           // the expert's h is complete once all of its gate/up items have counted in
           if (!wait_count(ra.ready + it.e, unsigned(s_a[it.e + 1] - s_a[it.e]), s_abort)) {
