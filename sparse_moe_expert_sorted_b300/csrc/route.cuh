@@ -36,6 +36,26 @@ struct RouteArgs {
   int32_t* perm_pp;
 };
 
+// Packed pairs of fp32 values (low half = first) and the packed IEEE operations on them.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // Warp-level top-k of one token's E logits.  Lane r ends up holding rank r
 // (value and id); the first k lanes write ids and weights.
 __device__ __forceinline__ void select_token(const RouteArgs& a, int t, int lane) {
@@ -118,6 +138,15 @@ route_logits_kernel(RouteArgs a, int fused_select) {
     for (int i = 0; i < EW; ++i)
 #pragma unroll
       for (int j = 0; j < TW; ++j) acc[i][j] = 0.f;
+    // Even TW: two tokens' accumulators share one packed f32x2 register, so one packed multiply
+    // and one packed add (each two independent IEEE fp32 operations, round to nearest) do the
+    // work of two; every accumulator still sees its products in the same order.
+    constexpr int TP = (TW % 2 == 0) ? TW / 2 : 1;
+    uint64_t acc2[EW][TP];
+#pragma unroll
+    for (int i = 0; i < EW; ++i)
+#pragma unroll
+      for (int q = 0; q < TP; ++q) acc2[i][q] = 0ull;
     for (int s0 = 0; s0 < S; s0 += RB) {
       uint4 wv[RB][EW], xv[RB][TW];
 #pragma unroll
@@ -139,20 +168,43 @@ route_logits_kernel(RouteArgs a, int fused_select) {
         if (s0 + b < S) {
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
+            if constexpr (TW % 2 == 0) {
+              uint64_t xp[TP];
 #pragma unroll
-            for (int i = 0; i < EW; ++i) {
-              const uint32_t ww = (&wv[b][i].x)[u >> 1];
-              const float wf = (u & 1) ? bf16_hi(ww) : bf16_lo(ww);
+              for (int q = 0; q < TP; ++q) {
+                const uint32_t x0 = (&xv[b][2 * q].x)[u >> 1], x1 = (&xv[b][2 * q + 1].x)[u >> 1];
+                xp[q] = f32x2_pack((u & 1) ? bf16_hi(x0) : bf16_lo(x0), (u & 1) ? bf16_hi(x1) : bf16_lo(x1));
+              }
 #pragma unroll
-              for (int j = 0; j < TW; ++j) {
-                const uint32_t xx = (&xv[b][j].x)[u >> 1];
-                const float xf = (u & 1) ? bf16_hi(xx) : bf16_lo(xx);
-                acc[i][j] = __fadd_rn(acc[i][j], __fmul_rn(xf, wf));
+              for (int i = 0; i < EW; ++i) {
+                const uint32_t ww = (&wv[b][i].x)[u >> 1];
+                const float wf = (u & 1) ? bf16_hi(ww) : bf16_lo(ww);
+                const uint64_t w2 = f32x2_pack(wf, wf);
+#pragma unroll
+                for (int q = 0; q < TP; ++q) acc2[i][q] = f32x2_add(acc2[i][q], f32x2_mul(xp[q], w2));
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < EW; ++i) {
+                const uint32_t ww = (&wv[b][i].x)[u >> 1];
+                const float wf = (u & 1) ? bf16_hi(ww) : bf16_lo(ww);
+#pragma unroll
+                for (int j = 0; j < TW; ++j) {
+                  const uint32_t xx = (&xv[b][j].x)[u >> 1];
+                  const float xf = (u & 1) ? bf16_hi(xx) : bf16_lo(xx);
+                  acc[i][j] = __fadd_rn(acc[i][j], __fmul_rn(xf, wf));
+                }
               }
             }
           }
         }
       }
+    }
+    if constexpr (TW % 2 == 0) {
+#pragma unroll
+      for (int i = 0; i < EW; ++i)
+#pragma unroll
+        for (int q = 0; q < TP; ++q) f32x2_unpack(acc2[i][q], acc[i][2 * q], acc[i][2 * q + 1]);
     }
 #pragma unroll
     for (int i = 0; i < EW; ++i)
