@@ -240,9 +240,11 @@ ftmoe_status ftmoe_permute(const ftmoe_layer_desc* desc, const int32_t* topk_ids
  *             otherwise: fused combine.  y_or_out is out fp32 [T][d], and
  *             w[p] * y is ADDED into it (zero it first, or pass a partial to merge)
  * Paths (ftmoe_expert_ffn_path tells which one a call takes):
- *   0  weight-only streaming on CUDA cores: x and h stay fp32, no activation
- *      quantisation.  Small T (decode), and every format the tensor-core path
- *      does not cover.
+ *   0  weight-only streaming: no activation quantisation.  For NVFP4 / MXFP4
+ *      weights the decoded weights meet x and h rounded to f16 in warp-level
+ *      MMAs with fp32 accumulation; BF16 and FP8 weights run on CUDA cores in
+ *      fp32.  Small T (decode), and every format the tensor-core path does not
+ *      cover.
  *   1  NVFP4 weights, T >= FTMOE_PREFILL_MIN_T, d % 256 == 0, ffn % 256 == 0:
  *      tcgen05 block-scaled tensor cores.  The gathered rows of x and h are
  *      quantised to NVFP4 by the rule of ftmoe_quantize_act.  Needs

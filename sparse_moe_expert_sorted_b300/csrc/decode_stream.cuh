@@ -442,11 +442,6 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-// Release add without a result: the earlier writes of this thread (and those ordered before
-// it by a __syncwarp) are visible before the add; the issuing warp does not wait.
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
   unsigned old;
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -485,26 +480,6 @@ __device__ __forceinline__ bool wait_count(const unsigned* v, unsigned target, v
     }
   }
   return true;
-}
-
-// Waits until the shared word *v equals want (bounded); false = gave up.  Whole warp: one
-// lane polls; warp-uniform result.
-__device__ __forceinline__ bool wait_smem_eq(volatile int* v, int want, volatile int* abort) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0 && *v != want) {
-    const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t it = 0; *v != want; ++it) {
-      if ((it & 63u) == 63u) {
-        if (*abort || globaltimer_ns() - t0 > kWaitLimitNs) {
-          ok = 0;
-          break;
-        }
-      }
-    }
-  }
-  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-  __syncwarp();
-  return ok != 0;
 }
 
 // Router logits of this CTA's experts e = b, b + G, ... for all T tokens, in order R (the
