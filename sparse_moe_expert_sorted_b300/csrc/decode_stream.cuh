@@ -442,6 +442,11 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
+// Release add without a result: the earlier writes of this thread, and those ordered before
+// it by a __syncwarp, are visible before the add.
+__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
   unsigned old;
   asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -676,10 +681,8 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
       }
     }
     __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      if (!grid_sync_mono(gsync, nullptr)) *s_abort = 1;
-    }
+    // (the sync's release add orders the CTA's logits, made visible to thread 0 by the barrier)
+    if (tid == 0 && !grid_sync_mono(gsync, nullptr)) *s_abort = 1;
     __syncthreads();
     if (*s_abort) {
       ok = false;
@@ -859,10 +862,7 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
             ++pend_n;
             if (q + 1 == count || item + step >= s_a[it.e + 1]) {
               __syncwarp();
-              if (lane == 0) {
-                __threadfence();
-                atomicAdd(ra.ready + it.e, pend_n);
-              }
+              if (lane == 0) red_add_release(ra.ready + it.e, pend_n);   // orders the warp's h stores
               pend_n = 0;
             }
           }
@@ -905,8 +905,7 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
               const unsigned old = atom_add_acq_rel(ra.merge + size_t(tk) * (a.d / 32) + it.n0, 1u);
               fin = int(old) + 1 == s_expect[tk];
             }
-            unsigned fm = __ballot_sync(0xFFFFFFFFu, fin);
-            if (fm) __threadfence();
+            unsigned fm = __ballot_sync(0xFFFFFFFFu, fin);   // (the acq_rel add acquired the others' y)
             while (fm) {
               const int tok = __ffs(fm) - 1;
               fm &= fm - 1;
