@@ -86,3 +86,31 @@ def test_short_workspace_and_null_pointers(L):
     d2 = ft.desc(8, 2, 256, 512, ft.NVFP4)
     st = L.ftmoe_expert_ffn(ctypes.byref(d2), ctypes.byref(w), None, 16, 4, 16, 16, None, 16, 16, 1 << 30, None)
     assert st == 1
+
+
+def _fake_weights(fmt, C, d, f, prepared):
+    # aligned fake device addresses: ftmoe_layer_path only checks them, never reads them
+    return ft.WeightsStruct(fmt, C, d, f, 0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000,
+                            0x8000 if prepared else None)
+
+
+def test_layer_path_choice_on_the_host(L):
+    """Which form ftmoe_layer_forward takes: one kernel for few tokens with 4-bit prepared
+    weights, separate steps otherwise, -1 for invalid arguments (host logic only)."""
+    dec = ft.desc(128, 8, 2048, 768, ft.NVFP4)
+    w = _fake_weights(ft.NVFP4, 128, 2048, 768, True)
+    for T in range(1, 9):
+        assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), T) == 1, T
+    assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), 9) == 0
+    assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), 8192) == 0
+    wn = _fake_weights(ft.NVFP4, 128, 2048, 768, False)
+    assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(wn), 1) == 0      # not prepared
+    stack = ft.desc(256, 6, 4096, 2048, ft.MXFP4)
+    ws = _fake_weights(ft.MXFP4, 225, 4096, 2048, True)
+    assert L.ftmoe_layer_path(ctypes.byref(stack), ctypes.byref(ws), 1) == 1
+    fp8 = ft.desc(256, 6, 4096, 2048, ft.FP8_B128)
+    w8 = _fake_weights(ft.FP8_B128, 256, 4096, 2048, True)
+    assert L.ftmoe_layer_path(ctypes.byref(fp8), ctypes.byref(w8), 1) == 0       # no 4-bit decode layout
+    assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), 0) == -1
+    wrong = _fake_weights(ft.MXFP4, 128, 2048, 768, True)                       # format differs from the layer
+    assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(wrong), 1) == -1
