@@ -18,7 +18,8 @@
 //   warp 17      epilogue: reduces the consumers' partial sums and writes h or y.
 // Work items, in order: phase A (gate/up) then phase B (down).  An item is
 // (expert, group of up to 8 tokens, block of rows); a stage is one item's rows.  Each CTA
-// takes a contiguous range of items, so consecutive items share the staged tokens.
+// takes a contiguous range of items, so consecutive items share the staged tokens (the
+// one-token layer call takes its gate/up items strided instead; see ROUTE below).
 //   phase A item: 16 gate + 16 up rows; the consumer warps split K.
 //   phase B item: 32 down rows; consumer warp w takes row tile w & 1 and K part w >> 1.
 // Prepared decode layout (ftmoe_prepare_weights), per slot: phase-A tiles (16 gate
@@ -45,7 +46,9 @@
 // of its experts (e = CTA, CTA + grid, ...) to shared memory (weights only); it then
 // computes their logits in the router's fixed order R, and after one grid sync every CTA
 // selects the top-k of all tokens itself (a rank count in shared memory) and sorts the
-// pairs by expert.  The combine is a merge: the down epilogue writes y per pair; the last
+// pairs by expert.  With one token, gate/up items go to CTAs strided by the grid (every
+// expert shares the staged x) so the first experts finish early, and down ranges run in
+// reverse CTA order.  The combine is a merge: the down epilogue writes y per pair; the last
 // of a token's resident pairs to finish a 32-column block sums w * y over the token's
 // ranks in ascending order (as ftmoe_combine does) and writes out in fp32 and bf16.
 #pragma once
