@@ -356,7 +356,8 @@ def bench_ours(args, rank, ws):
     value = tokens / (ms_max / 1e3)
     gpu_launches = launches_in_graph
 
-    fused = ft.layer_path(dsc, structs[0], T) == 1
+    lpath = ft.layer_path(dsc, structs[0], T)
+    fused = lpath in (1, 2)
     peaks, src = load_peaks()
     hbm = peaks["hbm_gbs"]
     eb = expert_bytes(wl)
@@ -367,7 +368,9 @@ def bench_ours(args, rank, ws):
         achieved = alg_bytes / (layer_us / 1e6) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(achieved / hbm, 4), "traffic": ncu_traffic(args.workload),
-                    "kernel": "ftmoe_layer_forward (one launch: sd_ffn_kernel with the router fused)",
+                    "kernel": "ftmoe_layer_forward (one launch: " + ("sl_layer_kernel, the one-token slice form"
+                                                                   if lpath == 2 else
+                                                                   "sd_ffn_kernel with the router fused") + ")",
                     "peak_source": src, "kernel_us": round(layer_us, 3), "alg_bytes_per_call": int(alg_bytes),
                     "mean_unique_experts": round(uniq_l, 2)}
         e2e = bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, min(K, 200), main)

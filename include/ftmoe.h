@@ -347,8 +347,11 @@ ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* lru, const int32_t* trace, int ste
  *      the decode path, the combine call otherwise).
  * ------------------------------------------------------------------------- */
 size_t ftmoe_layer_workspace_size(const ftmoe_layer_desc* desc, int T);
-/* 1 = ftmoe_layer_forward runs as one kernel for these weights and T, 0 = as separate
- * steps, -1 = invalid descriptor or weights. */
+/* Which form ftmoe_layer_forward takes for these weights and T: 0 = separate steps,
+ * 1 = one kernel (T <= 8), 2 = one kernel in the slice form (T = 1, d <= 2048: each
+ * gate/up item also applies its 16 columns of the down projection, and the CTAs' partial
+ * outputs are summed in a fixed order; the combine's sum regrouped, fp32 reassociation
+ * only), -1 = invalid descriptor or weights. */
 int ftmoe_layer_path(const ftmoe_layer_desc* desc, const ftmoe_weights* weights, int T);
 ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* desc, const ftmoe_weights* weights,
                                  const int32_t* slot_of, const uint16_t* x, const uint16_t* w_router,

@@ -433,6 +433,7 @@ struct SdRoute {
   float* ybuf;           // [T*k][d] workspace: y of each (token, rank) pair
   float* out_f32;        // [T][d]
   uint16_t* out_bf16;    // [T][d] or nullptr
+  float* part;           // [grid][d] workspace of the slice form: each CTA's partial output
 };
 
 __device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long* p, unsigned long long v) {
@@ -1110,6 +1111,416 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
       const float4 v = __ldcg(o + i);
       __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
       ob[i] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    }
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// One-token layer call, slice form (sl_layer_kernel).  Each gate/up item (16 rows of h) also
+// carries the down weights that read those 16 values: W_down[:, 16 n0 .. 16 n0 + 16) for all
+// d rows, one NVFP4 block (half an MXFP4 block) of K per row.  Right after the epilogue warp
+// has made the item's 16 h values, the consumer warps multiply them into the down slice
+// (warp w takes rows [w d/16, (w + 1) d/16)) and keep the CTA's partial output for their
+// rows in registers, across all of the CTA's items.  There is no down phase and no wait on
+// other CTAs' h; one grid sync at the end, then every CTA sums the partials of a block of
+// rows over the CTAs in CTA order (deterministic) and writes out in fp32 and bf16.
+// The combine weight and the block scale multiply the fp32 MMA result of each slice, so
+// out = sum over experts and slices of w * s * (W_slice h_slice): the combine's sum, regrouped.
+//
+// Prepared slice layout (after the decode layout, shapes with d <= 2048): per slot, per
+// slice n0: codes [d/16 row tiles][32 lanes][4 B] (lane (g, t) of a tile: bytes 2t and 2t + 1
+// of rows g and g + 8, i.e. K elements 4t .. 4t + 3, the MMA fragment of a K permutation
+// that the h operand follows too), then the rows' scales [d] (byte per row).
+__host__ __device__ inline bool sl_wanted(int d, int fmt) {
+  return (fmt == FTMOE_NVFP4 || fmt == FTMOE_MXFP4) && d % 256 == 0 && d / 256 <= 8;
+}
+__host__ __device__ inline int sl_slice_bytes(int d) { return 9 * d; }
+__host__ __device__ inline size_t sl_slot_bytes(int d, int f) { return size_t(f / kSdRowsA) * sl_slice_bytes(d); }
+
+// Canonical down codes + scales -> slice layout (one thread per output byte).
+__global__ void prep_slices_kernel(const uint8_t* down, const uint8_t* ds, int C, int d, int f, int fmt, uint8_t* out) {
+  const long long sb = sl_slice_bytes(d);
+  const long long per_slot = (long long)(f / kSdRowsA) * sb;
+  const long long total = per_slot * C;
+  for (long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x; o < total; o += (long long)gridDim.x * blockDim.x) {
+    const long long slot = o / per_slot;
+    const long long r = o % per_slot;
+    const long long n0 = r / sb, q = r % sb;
+    uint8_t v;
+    if (q < 8ll * d) {
+      const long long rt = q / 128;
+      const int L = int((q / 4) % 32), j = int(q % 4);
+      const int g = L >> 2, t = L & 3;
+      const long long row = rt * 16 + g + (j >= 2 ? 8 : 0);
+      const int byte = 2 * t + (j & 1);
+      v = down[(slot * d + row) * (f / 2) + 8 * n0 + byte];
+    } else {
+      const long long row = q - 8ll * d;
+      v = fmt == FTMOE_NVFP4 ? ds[(slot * d + row) * (f / 16) + n0] : ds[(slot * d + row) * (f / 32) + n0 / 2];
+    }
+    out[o] = v;
+  }
+}
+
+struct SlLayout {
+  int blk_a, off_d, stage_bytes, stages, estride, nred;
+  int off_x, off_red, off_rank, off_route, off_h, off_bar, smem;
+};
+__host__ __device__ inline SlLayout sl_layout(int E, int d, int fmt, int k, int max_smem) {
+  SlLayout L;
+  L.estride = E + 8;
+  L.blk_a = sd_block_bytes_a(d, fmt);
+  L.off_d = (L.blk_a + 127) / 128 * 128;
+  L.stage_bytes = L.off_d + (sl_slice_bytes(d) + 127) / 128 * 128;
+  L.nred = kSdCons * 2 * 16;                                   // one token
+  const int xbytes = ((d + 8) * 2 + 127) / 128 * 128;
+  const int red = kSdRedBufs * L.nred * 4;
+  const int info = (sd_info_ints(E) * 4 + 15) / 16 * 16;
+  const int rbytes = (sd_route_ints(E, 1, k) * 4 + 15) / 16 * 16;
+  const int fixed = xbytes + red + info + rbytes + 128 + 256;
+  L.stages = (max_smem - 1024 - fixed) / L.stage_bytes;
+  if (L.stages > 4) L.stages = 4;
+  L.off_x = L.stages * L.stage_bytes;
+  L.off_red = L.off_x + xbytes;
+  L.off_rank = L.off_red + red;
+  L.off_route = L.off_rank + info;
+  L.off_h = L.off_route + rbytes;
+  L.off_bar = L.off_h + 128;
+  L.smem = L.off_bar + 256 + 128;
+  return L;
+}
+// Whether the one-token layer call takes the slice form (the prepared slices exist for d).
+__host__ inline bool sl_supported(int E, int d, int f, int fmt, int k, int grid, int max_smem) {
+  if (!sl_wanted(d, fmt) || E > 1024 || (long long)E * E > (1ll << 22)) return false;
+  const SlLayout L = sl_layout(E, d, fmt, k, max_smem);
+  if (L.stages < 2) return false;
+  const long long rows = (E + grid - 1) / grid;
+  return rows * d * 2 <= (long long)L.stages * L.stage_bytes && f % kSdRowsA == 0;
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kSdThreads, 1)
+sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, const uint8_t* slices) {
+  extern __shared__ uint8_t sl_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sl_raw) + 127) & ~uintptr_t(127));
+  uint16_t* s_x = reinterpret_cast<uint16_t*>(sm + Ls.off_x);
+  float* s_red = reinterpret_cast<float*>(sm + Ls.off_red);   // [buffer][warp][m][16]
+  uint16_t* s_h = reinterpret_cast<uint16_t*>(sm + Ls.off_h);   // [buffer][16] f16
+  const int es = Ls.estride;
+  int* s_a = reinterpret_cast<int*>(sm + Ls.off_rank);
+  int* s_b = s_a + es;
+  int* s_lo = s_a + 2 * es;
+  int* s_cnt = s_a + 3 * es;
+  int* s_slot = s_a + 4 * es;
+  float* s_ts = reinterpret_cast<float*>(s_a + 5 * es);   // [E][3]
+  int* s_scan = s_a + 8 * es + 32;
+  float* s_logit = reinterpret_cast<float*>(sm + Ls.off_route);
+  const int P = a.k;                                       // one token
+  int* s_ids = reinterpret_cast<int*>(s_logit + a.E);
+  float* s_val = reinterpret_cast<float*>(s_ids + P);
+  float* s_wt = s_val + P;
+  int* s_sp = reinterpret_cast<int*>(s_wt + 2 * P);
+  int* s_off = s_sp + P + 1;
+  // barriers: full[4] 0, empty[4] 64 (16), router rows 128, red_full[2] 136 (16), red_empty[2]
+  // 152 (1), h_full[2] 168 (1), h_empty[2] 184 (16); flags at 208
+  const uint32_t bars = smem_u32(sm + Ls.off_bar);
+  const uint32_t red_full = bars + 136, red_empty = bars + 152, h_full = bars + 168, h_empty = bars + 184;
+  volatile int* s_flag = reinterpret_cast<volatile int*>(sm + Ls.off_bar + 208);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + Ls.off_bar + 212);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = Ls.stages;
+  const int G = gridDim.x, b = blockIdx.x;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bars + 8 * s, 1);
+      mbar_init(bars + 64 + 8 * s, kSdCons);
+    }
+    mbar_init(bars + 128, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(red_full + 8 * i, kSdCons);
+      mbar_init(red_empty + 8 * i, 1);
+      mbar_init(h_full + 8 * i, 1);
+      mbar_init(h_empty + 8 * i, kSdCons);
+    }
+    *s_flag = 1;
+    *s_abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  bool ok = true;
+  const int ne = a.E > b ? (a.E - b + G - 1) / G : 0;   // router rows of this CTA
+  if (tid == 0 && ne > 0) {
+    // router rows are weights: their copy may start before the previous kernel has finished
+    mbar_arrive_expect_tx(bars + 128, uint32_t(ne * a.d * 2));
+    for (int i = 0; i < ne; ++i)
+      bulk_load(smem_u32(sm + size_t(i) * a.d * 2), ra.wr + size_t(b + i * G) * a.d, uint32_t(a.d * 2), bars + 128);
+  }
+  pdl_wait();
+  if (a.slot_of)
+    for (int e = tid; e < a.E; e += kSdThreads) s_slot[e] = a.slot_of[e];
+  if (warp >= 1 && warp <= kSdCons && ne > 0) {
+    if (mbar_wait_warp(bars + 128, 0, s_abort)) {
+      sd_route_logits(a, ra, sm, ne, warp - 1, lane);
+    } else {
+      *s_abort = 1;
+    }
+  }
+  __syncthreads();
+  if (tid == 0 && !grid_sync_mono(gsync, nullptr)) *s_abort = 1;
+  __syncthreads();
+  if (*s_abort) {
+    ok = false;
+    if (tid == 0) set_dev_err(DEV_ERR_GRID_TIMEOUT);
+  }
+  sd_route_select(a, ra, s_logit, s_ids, s_val, s_wt, s_sp, s_off);
+  sd_items(a, s_off, a.slot_of ? s_slot : nullptr, 1, s_a, s_b, s_lo, s_cnt, s_slot, s_scan);   // all threads
+  const int NA = s_a[a.E];
+  const int count = NA > b ? (NA - b + G - 1) / G : 0;   // this CTA's items: b, b + G, ...
+  const int ua = a.f / kSdRowsA;
+  const size_t blk_a = size_t(Ls.blk_a);
+  const size_t slot_bytes = sd_slot_bytes(a.d, a.f, FMT);
+  const size_t slice_slot = sl_slot_bytes(a.d, a.f);
+  const int RP = a.d / 256;                                // row tiles per consumer warp
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    uint32_t stage = 0, ph = 0;
+    bool pok = ok;
+    SdItem it;
+    for (int q = 0; q < count && pok; ++q) {
+      sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, b + q * G, ua);
+      if (!mbar_wait_warp(bars + 64 + 8 * stage, ph ^ 1, s_abort)) {
+        pok = false;
+        break;
+      }
+      if (lane == 0) {
+        const uint32_t full = bars + 8 * stage;
+        mbar_arrive_expect_tx(full, uint32_t(blk_a + size_t(sl_slice_bytes(a.d))));
+        uint8_t* dst = sm + stage * Ls.stage_bytes;
+        bulk_load(smem_u32(dst), a.prep_dec + size_t(it.slot) * slot_bytes + size_t(it.n0) * blk_a, uint32_t(blk_a),
+                  full);
+        bulk_load(smem_u32(dst + Ls.off_d), slices + size_t(it.slot) * slice_slot + size_t(it.n0) * sl_slice_bytes(a.d),
+                  uint32_t(sl_slice_bytes(a.d)), full);
+      }
+      __syncwarp();
+      if (++stage == uint32_t(S)) {
+        stage = 0;
+        ph ^= 1;
+      }
+    }
+    if (!pok && ok && lane == 0) {
+      set_dev_err(DEV_ERR_TIMEOUT);
+      *s_abort = 1;
+    }
+    if (lane == 0) {
+      for (int i = 0; i < S; ++i) {
+        if (stage == 0) {
+          stage = S;
+          ph ^= 1;
+        }
+        --stage;
+        mbar_wait(bars + 8 * stage, ph, nullptr);
+      }
+      if (ne > 0 && !ok) mbar_wait(bars + 128, 0, nullptr);
+    }
+    return;
+  }
+
+  if (warp == kSdEpiWarp) {
+    // ---------------- epilogue warp: h of each item into s_h ----------------
+    sd_tensor_scales(a, s_a, s_slot, s_ts, lane, 32);
+    __syncwarp();
+    bool eok = ok;
+    SdItem it;
+    for (int q = 0; q < count; ++q) {
+      sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, b + q * G, ua);
+      if (q == 0) {
+        sd_work_sync();   // (the consumers stage x between these)
+        sd_work_sync();
+        if (!*s_flag) eok = false;
+      }
+      const int buf = q & 1, use = q >> 1;
+      if (eok && !mbar_wait_warp(red_full + 8 * buf, use & 1, s_abort)) {
+        eok = false;
+        *s_abort = 1;
+      }
+      float gs = 0.f, us = 0.f;
+      if (eok && lane < 16) {
+        const float* rb = s_red + buf * Ls.nred;
+#pragma unroll 4
+        for (int w = 0; w < kSdCons; ++w) {
+          gs += rb[(w * 2 + 0) * 16 + lane];
+          us += rb[(w * 2 + 1) * 16 + lane];
+        }
+      }
+      __syncwarp();
+      if (eok && lane == 0) mbar_arrive(red_empty + 8 * buf);
+      if (eok && !mbar_wait_warp(h_empty + 8 * buf, (use & 1) ^ 1, s_abort)) {
+        eok = false;
+        *s_abort = 1;
+      }
+      if (!eok) continue;
+      if (lane < 16) {
+        const float gg = gs * s_ts[3 * it.e + 0], uu = us * s_ts[3 * it.e + 1];
+        const float h = __fdividef(gg, 1.f + __expf(-gg)) * uu;
+        if (!isfinite(h)) set_dev_err(DEV_ERR_NONFINITE);
+        s_h[buf * 16 + lane] = __half_as_ushort(__float2half_rn(h));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(h_full + 8 * buf);
+    }
+    if (!eok && ok) set_dev_err(DEV_ERR_TIMEOUT);
+    sd_work_sync();   // (the consumers write their partial outputs and meet the grid between these)
+    sd_work_sync();
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int cw = warp - 1;
+  const int ct = tid - 32;
+  const int g = lane >> 2, t = lane & 3;
+  const int nsb = a.d / 64;
+  const int sb_lo = cw * nsb / kSdCons, sb_hi = (cw + 1) * nsb / kSdCons;
+  uint32_t stage = 0, ph = 0;
+  float yacc[8][2];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) yacc[i][0] = yacc[i][1] = 0.f;
+  // down slice of item j (stage dstage, expert de): fragments of h, 16 x 16 MMAs, scaled partials
+  auto down_part = [&](int j, uint32_t dstage, int de) {
+    const int buf = j & 1, use = j >> 1;
+    if (ok && !mbar_wait_warp(h_full + 8 * buf, use & 1, s_abort)) {
+      ok = false;
+      *s_abort = 1;
+    }
+    if (ok) {
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(s_h + buf * 16 + 4 * t);
+      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(s_h + buf * 16 + 4 * t + 2);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(h_empty + 8 * buf);
+      const uint8_t* dbase = sm + dstage * Ls.stage_bytes + Ls.off_d;
+      const uint8_t* sbase = dbase + 8 * a.d;
+      const int p = s_sp[s_lo[de]];                              // the token's pair with expert de
+      const float fac = s_wt[p] * s_ts[3 * de + 2];   // (tensor scales: loaded by the epilogue warp before the first barrier)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i < RP) {
+          const int rt = cw * RP + i;
+          const uint32_t c4 = *reinterpret_cast<const uint32_t*>(dbase + (rt * 32 + lane) * 4);
+          uint32_t fr[4];
+          e2m1x8_to_f16x8(c4, fr);
+          float dd[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_16816(dd, fr[0], fr[2], fr[1], fr[3], b0, b1);
+          const uint8_t s0 = sbase[rt * 16 + g], s1 = sbase[rt * 16 + g + 8];
+          const float f0 = FMT == FTMOE_NVFP4 ? e4m3_to_float(s0) : e8m0_to_float(s0);
+          const float f1 = FMT == FTMOE_NVFP4 ? e4m3_to_float(s1) : e8m0_to_float(s1);
+          yacc[i][0] = fmaf(f0 * fac, dd[0], yacc[i][0]);
+          yacc[i][1] = fmaf(f1 * fac, dd[2], yacc[i][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 64 + 8 * dstage);   // the stage is free
+  };
+  int pend_e = -1;
+  uint32_t pend_stage = 0;
+  SdItem it;
+  for (int q = 0; q < count; ++q) {
+    sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, b + q * G, ua);
+    if (q == 0) {
+      sd_work_sync();
+      if (!*s_flag) {
+        ok = false;
+        *s_abort = 1;
+      }
+      if (ok) {
+        const uint16_t* row = a.x;   // the one token
+        for (int c = ct; c < a.d / 8; c += kSdCons * 32) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + c);
+          uint4 hh;
+          hh.x = f16x2_of(bf16_lo(v.x), bf16_hi(v.x));
+          hh.y = f16x2_of(bf16_lo(v.y), bf16_hi(v.y));
+          hh.z = f16x2_of(bf16_lo(v.z), bf16_hi(v.z));
+          hh.w = f16x2_of(bf16_lo(v.w), bf16_hi(v.w));
+          *reinterpret_cast<uint4*>(s_x + 8 * c) = hh;
+        }
+      }
+      sd_work_sync();
+    }
+    // gate/up partials of item q
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    if (ok && !mbar_wait_warp(bars + 8 * stage, ph, s_abort)) {
+      ok = false;
+      *s_abort = 1;
+    }
+    if (ok) {
+      const uint8_t* base = sm + stage * Ls.stage_bytes;
+      const int cb = kSdRowsA * (a.d / 2), sbb = kSdRowsA * (a.d / (FMT == FTMOE_NVFP4 ? 16 : 32));
+      const uint8_t* const cbase[2] = {base, base + cb};
+      const uint8_t* const sbase[2] = {base + 2 * cb, base + 2 * cb + sbb};
+      sd_tiles_mma<FMT, 2, kSdRowsA>(cbase, sbase, g, s_x + 16 * t, sb_lo, sb_hi, t, acc);
+    }
+    const int buf = q & 1, use = q >> 1;
+    if (ok && !mbar_wait_warp(red_empty + 8 * buf, (use & 1) ^ 1, s_abort)) {
+      ok = false;
+      *s_abort = 1;
+    }
+    if (ok) {
+      float* rb = s_red + buf * Ls.nred;
+      if (t == 0) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          rb[(cw * 2 + m) * 16 + g] = acc[m][0];
+          rb[(cw * 2 + m) * 16 + g + 8] = acc[m][2];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(red_full + 8 * buf);
+    }
+    // down slice of the previous item (its h is ready by now, or soon)
+    if (q > 0) down_part(q - 1, pend_stage, pend_e);
+    pend_e = it.e;
+    pend_stage = stage;
+    if (++stage == uint32_t(S)) {
+      stage = 0;
+      ph ^= 1;
+    }
+  }
+  if (count > 0) down_part(count - 1, pend_stage, pend_e);
+  // this CTA's partial output (token 0 sits in column 0: lanes t == 0)
+  if (t == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i < RP) {
+        const int r0 = (cw * RP + i) * 16 + g;
+        ra.part[size_t(b) * a.d + r0] = yacc[i][0];
+        ra.part[size_t(b) * a.d + r0 + 8] = yacc[i][1];
+      }
+    }
+  }
+  if (!ok) set_dev_err(DEV_ERR_TIMEOUT);
+  sd_work_sync();
+  if (ct == 0) {
+    __threadfence();
+    if (!grid_sync_mono(gsync, s_abort)) {
+      *s_flag = 0;
+      set_dev_err(DEV_ERR_GRID_TIMEOUT);
+    }
+  }
+  sd_work_sync();
+  if (!*s_flag) return;
+  // rows [d b / G, d (b + 1) / G): sum the CTAs' partials in CTA order (lane-strided, then a
+  // fixed butterfly), write out
+  const int r_lo = int(unsigned(a.d) * unsigned(b) / unsigned(G)), r_hi = int(unsigned(a.d) * unsigned(b + 1) / unsigned(G));
+  for (int r = r_lo + cw; r < r_hi; r += kSdCons) {
+    float v = 0.f;
+    for (int c = lane; c < G; c += 32) v += __ldcg(ra.part + size_t(c) * a.d + r);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+    if (lane == 0) {
+      ra.out_f32[r] = v;
+      if (ra.out_bf16) ra.out_bf16[r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
     }
   }
 }

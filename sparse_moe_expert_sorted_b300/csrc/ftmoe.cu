@@ -172,9 +172,17 @@ size_t prep_prefill_bytes(const ftmoe_layer_desc* d, int C) {
   return align1k(prep_gate_up_bytes(d, C)) + prep_down_bytes(d, C);
 }
 size_t prep_decode_offset(const ftmoe_layer_desc* d, int C) { return align1k(prep_prefill_bytes(d, C)); }
+// decode layout [C][slot] then, where the one-token slice form applies (d <= 2048), the
+// down slices [C][slot]
+size_t prep_slices_bytes(const ftmoe_layer_desc* d, int C) {
+  return sl_wanted(d->d, d->fmt) ? size_t(C) * sl_slot_bytes(d->d, d->ffn) : 0;
+}
 size_t prep_decode_bytes(const ftmoe_layer_desc* d, int C) {
   if (d->fmt != FTMOE_NVFP4 && d->fmt != FTMOE_MXFP4) return 0;
-  return size_t(C) * sd_slot_bytes(d->d, d->ffn, d->fmt);
+  return size_t(C) * sd_slot_bytes(d->d, d->ffn, d->fmt) + prep_slices_bytes(d, C);
+}
+size_t prep_slices_offset(const ftmoe_layer_desc* d, int C) {
+  return prep_decode_offset(d, C) + size_t(C) * sd_slot_bytes(d->d, d->ffn, d->fmt);
 }
 size_t prep_bytes(const ftmoe_layer_desc* d, int C) {
   const size_t dec = prep_decode_bytes(d, C);
@@ -685,6 +693,11 @@ ftmoe_status ftmoe_prepare_weights(const ftmoe_layer_desc* d, const ftmoe_weight
                static_cast<const uint8_t*>(w->down), static_cast<const uint8_t*>(w->gate_scale),
                static_cast<const uint8_t*>(w->up_scale), static_cast<const uint8_t*>(w->down_scale), w->C, d->d,
                d->ffn, d->fmt, out + prep_decode_offset(d, w->C));
+    if (s != FTMOE_OK) return s;
+    if (prep_slices_bytes(d, w->C))
+      s = launch(prep_slices_kernel, dim3(grid), dim3(256), 0, st, static_cast<const uint8_t*>(w->down),
+                 static_cast<const uint8_t*>(w->down_scale), w->C, d->d, d->ffn, d->fmt,
+                 out + prep_slices_offset(d, w->C));
   }
   return s;
 }
@@ -807,7 +820,7 @@ namespace {
 // Fused decode layer (router, expert FFN and merge in one kernel): few tokens, a 4-bit
 // format with the prepared decode layout.  Its scratch: h (f16) | logits | ready | merge.
 struct FusedWs {
-  size_t h, logits, ready, merge, total;
+  size_t h, logits, ready, merge, part, total;
 };
 FusedWs fused_ws(const ftmoe_layer_desc* d, int T) {
   FusedWs F;
@@ -817,12 +830,26 @@ FusedWs fused_ws(const ftmoe_layer_desc* d, int T) {
   F.logits = o; o += align256(size_t(T) * d->E * 4);
   F.ready = o; o += align256(size_t(d->E) * 4);
   F.merge = o; o += align256(size_t(T) * (d->d / 32) * 4);
+  F.part = o; o += align256(size_t(num_sms()) * d->d * 4);   // slice form: each CTA's partial output
   F.total = o;
   return F;
 }
 bool layer_fused_ok(const ftmoe_layer_desc* d, const ftmoe_weights* w, int T) {
   if (ffn_path(d, T) != 0 || !w->prepared || !prep_decode_bytes(d, w->C)) return false;
   return sd_route_supported(d->E, d->d, d->ffn, d->fmt, T, d->k, num_sms(), max_smem_optin());
+}
+// the one-token slice form (down projection per gate/up item, no down phase)
+bool layer_slice_ok(const ftmoe_layer_desc* d, const ftmoe_weights* w, int T) {
+  if (T != 1 || ffn_path(d, T) != 0 || !w->prepared || !prep_slices_bytes(d, w->C)) return false;
+  return sl_supported(d->E, d->d, d->ffn, d->fmt, d->k, num_sms(), max_smem_optin());
+}
+template <int FMT>
+ftmoe_status layer_slice_launch(const FfnArgs& a, const SdRoute& r, void* hdr, const uint8_t* slices,
+                                cudaStream_t st) {
+  const SlLayout Ls = sl_layout(a.E, a.d, FMT, a.k, max_smem_optin());
+  if (resident_ctas(sl_layer_kernel<FMT>, kSdThreads, size_t(Ls.smem)) < 1) return FTMOE_ERR_CUDA;
+  unsigned long long* gs = reinterpret_cast<unsigned long long*>(static_cast<char*>(hdr) + kWsGridSync);
+  return launch(sl_layer_kernel<FMT>, dim3(num_sms()), dim3(kSdThreads), size_t(Ls.smem), st, a, Ls, r, gs, slices);
 }
 template <int FMT>
 ftmoe_status layer_fused_launch(const FfnArgs& a, const SdRoute& r, void* hdr, cudaStream_t st) {
@@ -866,7 +893,8 @@ size_t ftmoe_layer_workspace_size(const ftmoe_layer_desc* d, int T) {
 
 int ftmoe_layer_path(const ftmoe_layer_desc* d, const ftmoe_weights* w, int T) {
   if (!desc_ok(d) || T < 1 || T > kMaxT || !weights_ok(d, w)) return -1;
-  return layer_fused_ok(d, w, T) ? 1 : 0;
+  if (!layer_fused_ok(d, w, T)) return 0;
+  return layer_slice_ok(d, w, T) ? 2 : 1;
 }
 
 ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights* w, const int32_t* slot_of,
@@ -911,6 +939,12 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
     r.ybuf = y;
     r.out_f32 = out_f32;
     r.out_bf16 = out_bf16;
+    r.part = reinterpret_cast<float*>(sc + F.part);
+    if (layer_slice_ok(d, w, T)) {
+      const uint8_t* slices = static_cast<const uint8_t*>(w->prepared) + prep_slices_offset(d, w->C);
+      return d->fmt == FTMOE_NVFP4 ? layer_slice_launch<FTMOE_NVFP4>(a, r, base, slices, st)
+                                   : layer_slice_launch<FTMOE_MXFP4>(a, r, base, slices, st);
+    }
     return d->fmt == FTMOE_NVFP4 ? layer_fused_launch<FTMOE_NVFP4>(a, r, base, st)
                                  : layer_fused_launch<FTMOE_MXFP4>(a, r, base, st);
   }

@@ -99,7 +99,8 @@ def test_layer_path_choice_on_the_host(L):
     weights, separate steps otherwise, -1 for invalid arguments (host logic only)."""
     dec = ft.desc(128, 8, 2048, 768, ft.NVFP4)
     w = _fake_weights(ft.NVFP4, 128, 2048, 768, True)
-    for T in range(1, 9):
+    assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), 1) == 2     # one token: the slice form
+    for T in range(2, 9):
         assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), T) == 1, T
     assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), 9) == 0
     assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), 8192) == 0
@@ -107,7 +108,7 @@ def test_layer_path_choice_on_the_host(L):
     assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(wn), 1) == 0      # not prepared
     stack = ft.desc(256, 6, 4096, 2048, ft.MXFP4)
     ws = _fake_weights(ft.MXFP4, 225, 4096, 2048, True)
-    assert L.ftmoe_layer_path(ctypes.byref(stack), ctypes.byref(ws), 1) == 1
+    assert L.ftmoe_layer_path(ctypes.byref(stack), ctypes.byref(ws), 1) == 1   # d 4096: no slice layout
     fp8 = ft.desc(256, 6, 4096, 2048, ft.FP8_B128)
     w8 = _fake_weights(ft.FP8_B128, 256, 4096, 2048, True)
     assert L.ftmoe_layer_path(ctypes.byref(fp8), ctypes.byref(w8), 1) == 0       # no 4-bit decode layout
