@@ -348,7 +348,8 @@ ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* lru, const int32_t* trace, int ste
  * ------------------------------------------------------------------------- */
 size_t ftmoe_layer_workspace_size(const ftmoe_layer_desc* desc, int T);
 /* Which form ftmoe_layer_forward takes for these weights and T: 0 = separate steps,
- * 1 = one kernel (T <= 8), 2 = one kernel in the slice form (T = 1, d <= 2048: each
+ * 1 = one kernel (T <= 8), 2 = one kernel in the slice form (d <= 2048 and T = 1, or
+ * T <= 8 with NVFP4 weights: each
  * gate/up item also applies its 16 columns of the down projection, and the CTAs' partial
  * outputs are summed in a fixed order; the combine's sum regrouped, fp32 reassociation
  * only), -1 = invalid descriptor or weights. */

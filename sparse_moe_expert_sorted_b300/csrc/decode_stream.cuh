@@ -1164,21 +1164,23 @@ __global__ void prep_slices_kernel(const uint8_t* down, const uint8_t* ds, int C
 }
 
 struct SlLayout {
-  int blk_a, off_d, stage_bytes, stages, estride, nred;
+  int blk_a, off_d, stage_bytes, stages, estride, nred, xr;
   int off_x, off_red, off_rank, off_route, off_h, off_bar, smem;
 };
-__host__ __device__ inline SlLayout sl_layout(int E, int d, int fmt, int k, int max_smem) {
+// T <= 8 tokens: one token group per expert (xr = T staged x rows)
+__host__ __device__ inline SlLayout sl_layout(int E, int d, int fmt, int T, int k, int max_smem) {
   SlLayout L;
+  L.xr = T;
   L.estride = E + 8;
   L.blk_a = sd_block_bytes_a(d, fmt);
   L.off_d = (L.blk_a + 127) / 128 * 128;
   L.stage_bytes = L.off_d + (sl_slice_bytes(d) + 127) / 128 * 128;
-  L.nred = kSdCons * 2 * 16;                                   // one token
-  const int xbytes = ((d + 8) * 2 + 127) / 128 * 128;
+  L.nred = kSdCons * 2 * 16 * T;
+  const int xbytes = (T * (d + 8) * 2 + 127) / 128 * 128;
   const int red = kSdRedBufs * L.nred * 4;
   const int info = (sd_info_ints(E) * 4 + 15) / 16 * 16;
-  const int rbytes = (sd_route_ints(E, 1, k) * 4 + 15) / 16 * 16;
-  const int fixed = xbytes + red + info + rbytes + 128 + 256;
+  const int rbytes = (sd_route_ints(E, T, k) * 4 + 15) / 16 * 16;
+  const int fixed = xbytes + red + info + rbytes + 512 + 256;
   L.stages = (max_smem - 1024 - fixed) / L.stage_bytes;
   if (L.stages > 4) L.stages = 4;
   L.off_x = L.stages * L.stage_bytes;
@@ -1186,27 +1188,28 @@ __host__ __device__ inline SlLayout sl_layout(int E, int d, int fmt, int k, int 
   L.off_rank = L.off_red + red;
   L.off_route = L.off_rank + info;
   L.off_h = L.off_route + rbytes;
-  L.off_bar = L.off_h + 128;
+  L.off_bar = L.off_h + 512;                                   // h: [2 buffers][8 token columns][16] f16
   L.smem = L.off_bar + 256 + 128;
   return L;
 }
-// Whether the one-token layer call takes the slice form (the prepared slices exist for d).
-__host__ inline bool sl_supported(int E, int d, int f, int fmt, int k, int grid, int max_smem) {
-  if (!sl_wanted(d, fmt) || E > 1024 || (long long)E * E > (1ll << 22)) return false;
-  const SlLayout L = sl_layout(E, d, fmt, k, max_smem);
+// Whether a layer call of T tokens takes the slice form (the prepared slices exist for d).
+__host__ inline bool sl_supported(int E, int d, int f, int fmt, int T, int k, int grid, int max_smem) {
+  if (!sl_wanted(d, fmt) || T < 1 || T > kSdRouteMaxT || E > 1024 || (long long)T * E * E > (1ll << 22)) return false;
+  const SlLayout L = sl_layout(E, d, fmt, T, k, max_smem);
   if (L.stages < 2) return false;
   const long long rows = (E + grid - 1) / grid;
   return rows * d * 2 <= (long long)L.stages * L.stage_bytes && f % kSdRowsA == 0;
 }
 
-template <int FMT>
+// NCOL: token columns a lane keeps partial outputs for (1 when T = 1: column 0 only; 2 otherwise)
+template <int FMT, int NCOL>
 __global__ void __launch_bounds__(kSdThreads, 1)
 sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, const uint8_t* slices) {
   extern __shared__ uint8_t sl_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sl_raw) + 127) & ~uintptr_t(127));
   uint16_t* s_x = reinterpret_cast<uint16_t*>(sm + Ls.off_x);
   float* s_red = reinterpret_cast<float*>(sm + Ls.off_red);   // [buffer][warp][m][16]
-  uint16_t* s_h = reinterpret_cast<uint16_t*>(sm + Ls.off_h);   // [buffer][16] f16
+  uint16_t* s_h = reinterpret_cast<uint16_t*>(sm + Ls.off_h);   // [buffer][token column 8][16] f16
   const int es = Ls.estride;
   int* s_a = reinterpret_cast<int*>(sm + Ls.off_rank);
   int* s_b = s_a + es;
@@ -1214,14 +1217,16 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
   int* s_cnt = s_a + 3 * es;
   int* s_slot = s_a + 4 * es;
   float* s_ts = reinterpret_cast<float*>(s_a + 5 * es);   // [E][3]
+  int* s_tok = s_a + 8 * es;                               // token group: token of each row
   int* s_scan = s_a + 8 * es + 32;
   float* s_logit = reinterpret_cast<float*>(sm + Ls.off_route);
-  const int P = a.k;                                       // one token
-  int* s_ids = reinterpret_cast<int*>(s_logit + a.E);
+  const int P = a.T * a.k;
+  int* s_ids = reinterpret_cast<int*>(s_logit + a.T * a.E);
   float* s_val = reinterpret_cast<float*>(s_ids + P);
   float* s_wt = s_val + P;
   int* s_sp = reinterpret_cast<int*>(s_wt + 2 * P);
-  int* s_off = s_sp + P + 1;
+  int* s_off = s_sp + P + a.T;
+  const int xr = Ls.xr;
   // barriers: full[4] 0, empty[4] 64 (16), router rows 128, red_full[2] 136 (16), red_empty[2]
   // 152 (1), h_full[2] 168 (1), h_empty[2] 184 (16); flags at 208
   const uint32_t bars = smem_u32(sm + Ls.off_bar);
@@ -1275,9 +1280,14 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
     if (tid == 0) set_dev_err(DEV_ERR_GRID_TIMEOUT);
   }
   sd_route_select(a, ra, s_logit, s_ids, s_val, s_wt, s_sp, s_off);
-  sd_items(a, s_off, a.slot_of ? s_slot : nullptr, 1, s_a, s_b, s_lo, s_cnt, s_slot, s_scan);   // all threads
+  sd_items(a, s_off, a.slot_of ? s_slot : nullptr, xr, s_a, s_b, s_lo, s_cnt, s_slot, s_scan);   // all threads
   const int NA = s_a[a.E];
-  const int count = NA > b ? (NA - b + G - 1) / G : 0;   // this CTA's items: b, b + G, ...
+  // items: one token takes b, b + G, ... (every expert shares the staged x); more tokens take a
+  // contiguous range (x is restaged per expert)
+  const bool strided = a.T == 1;
+  const int a_lo = int(unsigned(NA) * unsigned(b) / unsigned(G)), a_hi = int(unsigned(NA) * unsigned(b + 1) / unsigned(G));
+  const int first = strided ? b : a_lo, step = strided ? G : 1;
+  const int count = strided ? (NA > b ? (NA - b + G - 1) / G : 0) : a_hi - a_lo;
   const int ua = a.f / kSdRowsA;
   const size_t blk_a = size_t(Ls.blk_a);
   const size_t slot_bytes = sd_slot_bytes(a.d, a.f, FMT);
@@ -1290,7 +1300,7 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
     bool pok = ok;
     SdItem it;
     for (int q = 0; q < count && pok; ++q) {
-      sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, b + q * G, ua);
+      sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, first + q * step, ua);
       if (!mbar_wait_warp(bars + 64 + 8 * stage, ph ^ 1, s_abort)) {
         pok = false;
         break;
@@ -1334,25 +1344,34 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
     __syncwarp();
     bool eok = ok;
     SdItem it;
+    int staged_e = -1;
     for (int q = 0; q < count; ++q) {
-      sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, b + q * G, ua);
-      if (q == 0) {
-        sd_work_sync();   // (the consumers stage x between these)
+      sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, first + q * step, ua);
+      if (strided ? q == 0 : it.e != staged_e) {
+        sd_work_sync();   // (the consumers stage x and the token group between these)
         sd_work_sync();
         if (!*s_flag) eok = false;
+        staged_e = it.e;
       }
+      const int n = min(xr, it.cnt);
       const int buf = q & 1, use = q >> 1;
       if (eok && !mbar_wait_warp(red_full + 8 * buf, use & 1, s_abort)) {
         eok = false;
         *s_abort = 1;
       }
-      float gs = 0.f, us = 0.f;
-      if (eok && lane < 16) {
-        const float* rb = s_red + buf * Ls.nred;
+      // lane: row lane & 15, group rows (lane >> 4) + 2j
+      float gs[4], us[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        gs[j] = us[j] = 0.f;
+        const int tok = (lane >> 4) + 2 * j;
+        if (eok && tok < n) {
+          const float* rb = s_red + buf * Ls.nred;
 #pragma unroll 4
-        for (int w = 0; w < kSdCons; ++w) {
-          gs += rb[(w * 2 + 0) * 16 + lane];
-          us += rb[(w * 2 + 1) * 16 + lane];
+          for (int w = 0; w < kSdCons; ++w) {
+            gs[j] += rb[((w * 2 + 0) * 16 + (lane & 15)) * xr + tok];
+            us[j] += rb[((w * 2 + 1) * 16 + (lane & 15)) * xr + tok];
+          }
         }
       }
       __syncwarp();
@@ -1362,11 +1381,19 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
         *s_abort = 1;
       }
       if (!eok) continue;
-      if (lane < 16) {
-        const float gg = gs * s_ts[3 * it.e + 0], uu = us * s_ts[3 * it.e + 1];
-        const float h = __fdividef(gg, 1.f + __expf(-gg)) * uu;
-        if (!isfinite(h)) set_dev_err(DEV_ERR_NONFINITE);
-        s_h[buf * 16 + lane] = __half_as_ushort(__float2half_rn(h));
+      // h by batch-token column (zeros for tokens this expert does not serve)
+      uint16_t* hb = s_h + buf * 128;
+      for (int i = lane; i < 128; i += 32) hb[i] = 0;
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int tok = (lane >> 4) + 2 * j;
+        if (tok < n) {
+          const float gg = gs[j] * s_ts[3 * it.e + 0], uu = us[j] * s_ts[3 * it.e + 1];
+          const float h = __fdividef(gg, 1.f + __expf(-gg)) * uu;
+          if (!isfinite(h)) set_dev_err(DEV_ERR_NONFINITE);
+          hb[s_tok[tok] * 16 + (lane & 15)] = __half_as_ushort(__float2half_rn(h));
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(h_full + 8 * buf);
@@ -1384,25 +1411,29 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
   const int nsb = a.d / 64;
   const int sb_lo = cw * nsb / kSdCons, sb_hi = (cw + 1) * nsb / kSdCons;
   uint32_t stage = 0, ph = 0;
-  float yacc[8][2];
+  float yacc[8][2][NCOL];   // [row tile][row g, g + 8][token 2t + j]
 #pragma unroll
-  for (int i = 0; i < 8; ++i) yacc[i][0] = yacc[i][1] = 0.f;
-  // down slice of item j (stage dstage, expert de): fragments of h, 16 x 16 MMAs, scaled partials
-  auto down_part = [&](int j, uint32_t dstage, int de) {
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+      for (int j = 0; j < NCOL; ++j) yacc[i][h2][j] = 0.f;
+  // down slice of item j (stage dstage, expert de; this lane's two token columns 2t, 2t + 1
+  // carry combine weights w0, w1): fragments of h, 16 x 16 MMAs, scaled partials
+  auto down_part = [&](int j, uint32_t dstage, int de, float w0, float w1) {
     const int buf = j & 1, use = j >> 1;
     if (ok && !mbar_wait_warp(h_full + 8 * buf, use & 1, s_abort)) {
       ok = false;
       *s_abort = 1;
     }
     if (ok) {
-      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(s_h + buf * 16 + 4 * t);
-      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(s_h + buf * 16 + 4 * t + 2);
+      const uint32_t b0 = *reinterpret_cast<const uint32_t*>(s_h + buf * 128 + g * 16 + 4 * t);
+      const uint32_t b1 = *reinterpret_cast<const uint32_t*>(s_h + buf * 128 + g * 16 + 4 * t + 2);
       __syncwarp();
       if (lane == 0) mbar_arrive(h_empty + 8 * buf);
       const uint8_t* dbase = sm + dstage * Ls.stage_bytes + Ls.off_d;
       const uint8_t* sbase = dbase + 8 * a.d;
-      const int p = s_sp[s_lo[de]];                              // the token's pair with expert de
-      const float fac = s_wt[p] * s_ts[3 * de + 2];   // (tensor scales: loaded by the epilogue warp before the first barrier)
+      const float tsd = s_ts[3 * de + 2];   // (tensor scales: loaded by the epilogue warp before the first barrier)
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (i < RP) {
@@ -1413,40 +1444,59 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
           float dd[4] = {0.f, 0.f, 0.f, 0.f};
           mma_16816(dd, fr[0], fr[2], fr[1], fr[3], b0, b1);
           const uint8_t s0 = sbase[rt * 16 + g], s1 = sbase[rt * 16 + g + 8];
-          const float f0 = FMT == FTMOE_NVFP4 ? e4m3_to_float(s0) : e8m0_to_float(s0);
-          const float f1 = FMT == FTMOE_NVFP4 ? e4m3_to_float(s1) : e8m0_to_float(s1);
-          yacc[i][0] = fmaf(f0 * fac, dd[0], yacc[i][0]);
-          yacc[i][1] = fmaf(f1 * fac, dd[2], yacc[i][1]);
+          const float f0 = (FMT == FTMOE_NVFP4 ? e4m3_to_float(s0) : e8m0_to_float(s0)) * tsd;
+          const float f1 = (FMT == FTMOE_NVFP4 ? e4m3_to_float(s1) : e8m0_to_float(s1)) * tsd;
+          yacc[i][0][0] = fmaf(f0 * w0, dd[0], yacc[i][0][0]);     // row g, token 2t
+          yacc[i][1][0] = fmaf(f1 * w0, dd[2], yacc[i][1][0]);     // row g + 8, token 2t
+          if (NCOL == 2) {
+            yacc[i][0][NCOL - 1] = fmaf(f0 * w1, dd[1], yacc[i][0][NCOL - 1]);   // row g, token 2t + 1
+            yacc[i][1][NCOL - 1] = fmaf(f1 * w1, dd[3], yacc[i][1][NCOL - 1]);   // row g + 8, token 2t + 1
+          }
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 64 + 8 * dstage);   // the stage is free
   };
-  int pend_e = -1;
+  int pend_e = -1, staged_e = -1;
   uint32_t pend_stage = 0;
+  float pend_w0 = 0.f, pend_w1 = 0.f;
+  const int st_x = a.d + 8;
   SdItem it;
   for (int q = 0; q < count; ++q) {
-    sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, b + q * G, ua);
-    if (q == 0) {
+    sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, first + q * step, ua);
+    const int n = min(xr, it.cnt);
+    if (strided ? q == 0 : it.e != staged_e) {
+      // the expert's token group: x rows (f16) and tokens (one token: staged once)
       sd_work_sync();
       if (!*s_flag) {
         ok = false;
         *s_abort = 1;
       }
+      if (ct < n) s_tok[ct] = s_sp[it.lo + ct] / a.k;
       if (ok) {
-        const uint16_t* row = a.x;   // the one token
-        for (int c = ct; c < a.d / 8; c += kSdCons * 32) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + c);
+        const int per = a.d / 8;
+        for (int c = ct; c < n * per; c += kSdCons * 32) {
+          const int qq = c / per, cc = c - qq * per;
+          const uint16_t* row = a.x + size_t(s_sp[it.lo + qq] / a.k) * a.d;
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + cc);
           uint4 hh;
           hh.x = f16x2_of(bf16_lo(v.x), bf16_hi(v.x));
           hh.y = f16x2_of(bf16_lo(v.y), bf16_hi(v.y));
           hh.z = f16x2_of(bf16_lo(v.z), bf16_hi(v.z));
           hh.w = f16x2_of(bf16_lo(v.w), bf16_hi(v.w));
-          *reinterpret_cast<uint4*>(s_x + 8 * c) = hh;
+          *reinterpret_cast<uint4*>(s_x + qq * st_x + 8 * cc) = hh;
         }
       }
+      staged_e = it.e;
       sd_work_sync();
+    }
+    // this lane's token columns 2t, 2t + 1: the expert's combine weight for each (0 if it does not serve it)
+    float w0 = 0.f, w1 = 0.f;
+    for (int j = 0; j < n; ++j) {
+      const int pj = s_sp[it.lo + j], tk = pj / a.k;
+      if (tk == 2 * t) w0 = s_wt[pj];
+      if (tk == 2 * t + 1) w1 = s_wt[pj];
     }
     // gate/up partials of item q
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -1459,7 +1509,8 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
       const int cb = kSdRowsA * (a.d / 2), sbb = kSdRowsA * (a.d / (FMT == FTMOE_NVFP4 ? 16 : 32));
       const uint8_t* const cbase[2] = {base, base + cb};
       const uint8_t* const sbase[2] = {base + 2 * cb, base + 2 * cb + sbb};
-      sd_tiles_mma<FMT, 2, kSdRowsA>(cbase, sbase, g, s_x + 16 * t, sb_lo, sb_hi, t, acc);
+      // MMA token column g: rows past the staged ones read the last staged row (results unused)
+      sd_tiles_mma<FMT, 2, kSdRowsA>(cbase, sbase, g, s_x + min(g, xr - 1) * st_x + 16 * t, sb_lo, sb_hi, t, acc);
     }
     const int buf = q & 1, use = q >> 1;
     if (ok && !mbar_wait_warp(red_empty + 8 * buf, (use & 1) ^ 1, s_abort)) {
@@ -1468,34 +1519,46 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
     }
     if (ok) {
       float* rb = s_red + buf * Ls.nred;
-      if (t == 0) {
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          rb[(cw * 2 + m) * 16 + g] = acc[m][0];
-          rb[(cw * 2 + m) * 16 + g + 8] = acc[m][2];
+      for (int m = 0; m < 2; ++m) {
+        float* my = rb + ((cw * 2 + m) * 16) * xr;
+        if (2 * t < xr) {
+          my[g * xr + 2 * t] = acc[m][0];
+          my[(g + 8) * xr + 2 * t] = acc[m][2];
+        }
+        if (2 * t + 1 < xr) {
+          my[g * xr + 2 * t + 1] = acc[m][1];
+          my[(g + 8) * xr + 2 * t + 1] = acc[m][3];
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(red_full + 8 * buf);
     }
     // down slice of the previous item (its h is ready by now, or soon)
-    if (q > 0) down_part(q - 1, pend_stage, pend_e);
+    if (q > 0) down_part(q - 1, pend_stage, pend_e, pend_w0, pend_w1);
     pend_e = it.e;
     pend_stage = stage;
+    pend_w0 = w0;
+    pend_w1 = w1;
     if (++stage == uint32_t(S)) {
       stage = 0;
       ph ^= 1;
     }
   }
-  if (count > 0) down_part(count - 1, pend_stage, pend_e);
-  // this CTA's partial output (token 0 sits in column 0: lanes t == 0)
-  if (t == 0) {
+  if (count > 0) down_part(count - 1, pend_stage, pend_e, pend_w0, pend_w1);
+  // this CTA's partial output [token][row]: this lane holds tokens 2t, 2t + 1 of rows g, g + 8
+  float* pb = ra.part + size_t(b) * a.T * a.d;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i < RP) {
-        const int r0 = (cw * RP + i) * 16 + g;
-        ra.part[size_t(b) * a.d + r0] = yacc[i][0];
-        ra.part[size_t(b) * a.d + r0 + 8] = yacc[i][1];
+  for (int i = 0; i < 8; ++i) {
+    if (i < RP) {
+      const int r0 = (cw * RP + i) * 16 + g;
+      if (2 * t < a.T) {
+        pb[size_t(2 * t) * a.d + r0] = yacc[i][0][0];
+        pb[size_t(2 * t) * a.d + r0 + 8] = yacc[i][1][0];
+      }
+      if (NCOL == 2 && 2 * t + 1 < a.T) {
+        pb[size_t(2 * t + 1) * a.d + r0] = yacc[i][0][NCOL - 1];
+        pb[size_t(2 * t + 1) * a.d + r0 + 8] = yacc[i][1][NCOL - 1];
       }
     }
   }
@@ -1510,17 +1573,18 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
   }
   sd_work_sync();
   if (!*s_flag) return;
-  // rows [d b / G, d (b + 1) / G): sum the CTAs' partials in CTA order (lane-strided, then a
-  // fixed butterfly), write out
-  const int r_lo = int(unsigned(a.d) * unsigned(b) / unsigned(G)), r_hi = int(unsigned(a.d) * unsigned(b + 1) / unsigned(G));
-  for (int r = r_lo + cw; r < r_hi; r += kSdCons) {
+  // outputs [T d b / G, T d (b + 1) / G) of out [T][d]: sum the CTAs' partials in CTA order
+  // (lane-strided, then a fixed butterfly), write out
+  const unsigned nout = unsigned(a.T) * unsigned(a.d);
+  const int o_lo = int(nout * unsigned(b) / unsigned(G)), o_hi = int(nout * unsigned(b + 1) / unsigned(G));
+  for (int o = o_lo + cw; o < o_hi; o += kSdCons) {
     float v = 0.f;
-    for (int c = lane; c < G; c += 32) v += __ldcg(ra.part + size_t(c) * a.d + r);
+    for (int c = lane; c < G; c += 32) v += __ldcg(ra.part + size_t(c) * nout + o);
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
     if (lane == 0) {
-      ra.out_f32[r] = v;
-      if (ra.out_bf16) ra.out_bf16[r] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      ra.out_f32[o] = v;
+      if (ra.out_bf16) ra.out_bf16[o] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
     }
   }
 }

@@ -830,7 +830,7 @@ FusedWs fused_ws(const ftmoe_layer_desc* d, int T) {
   F.logits = o; o += align256(size_t(T) * d->E * 4);
   F.ready = o; o += align256(size_t(d->E) * 4);
   F.merge = o; o += align256(size_t(T) * (d->d / 32) * 4);
-  F.part = o; o += align256(size_t(num_sms()) * d->d * 4);   // slice form: each CTA's partial output
+  F.part = o; o += align256(size_t(num_sms()) * T * d->d * 4);   // slice form: each CTA's partial output
   F.total = o;
   return F;
 }
@@ -840,16 +840,19 @@ bool layer_fused_ok(const ftmoe_layer_desc* d, const ftmoe_weights* w, int T) {
 }
 // the one-token slice form (down projection per gate/up item, no down phase)
 bool layer_slice_ok(const ftmoe_layer_desc* d, const ftmoe_weights* w, int T) {
-  if (T != 1 || ffn_path(d, T) != 0 || !w->prepared || !prep_slices_bytes(d, w->C)) return false;
-  return sl_supported(d->E, d->d, d->ffn, d->fmt, d->k, num_sms(), max_smem_optin());
+  if (T < 1 || T > kSdRouteMaxT || ffn_path(d, T) != 0 || !w->prepared || !prep_slices_bytes(d, w->C)) return false;
+  // more than one token: NVFP4 only (the MXFP4 instance with two token columns runs out of registers)
+  if (T > 1 && d->fmt != FTMOE_NVFP4) return false;
+  return sl_supported(d->E, d->d, d->ffn, d->fmt, T, d->k, num_sms(), max_smem_optin());
 }
-template <int FMT>
+template <int FMT, int NCOL>
 ftmoe_status layer_slice_launch(const FfnArgs& a, const SdRoute& r, void* hdr, const uint8_t* slices,
                                 cudaStream_t st) {
-  const SlLayout Ls = sl_layout(a.E, a.d, FMT, a.k, max_smem_optin());
-  if (resident_ctas(sl_layer_kernel<FMT>, kSdThreads, size_t(Ls.smem)) < 1) return FTMOE_ERR_CUDA;
+  const SlLayout Ls = sl_layout(a.E, a.d, FMT, a.T, a.k, max_smem_optin());
+  if (resident_ctas(sl_layer_kernel<FMT, NCOL>, kSdThreads, size_t(Ls.smem)) < 1) return FTMOE_ERR_CUDA;
   unsigned long long* gs = reinterpret_cast<unsigned long long*>(static_cast<char*>(hdr) + kWsGridSync);
-  return launch(sl_layer_kernel<FMT>, dim3(num_sms()), dim3(kSdThreads), size_t(Ls.smem), st, a, Ls, r, gs, slices);
+  return launch(sl_layer_kernel<FMT, NCOL>, dim3(num_sms()), dim3(kSdThreads), size_t(Ls.smem), st, a, Ls, r, gs,
+                slices);
 }
 template <int FMT>
 ftmoe_status layer_fused_launch(const FfnArgs& a, const SdRoute& r, void* hdr, cudaStream_t st) {
@@ -942,8 +945,9 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
     r.part = reinterpret_cast<float*>(sc + F.part);
     if (layer_slice_ok(d, w, T)) {
       const uint8_t* slices = static_cast<const uint8_t*>(w->prepared) + prep_slices_offset(d, w->C);
-      return d->fmt == FTMOE_NVFP4 ? layer_slice_launch<FTMOE_NVFP4>(a, r, base, slices, st)
-                                   : layer_slice_launch<FTMOE_MXFP4>(a, r, base, slices, st);
+      if (T > 1) return layer_slice_launch<FTMOE_NVFP4, 2>(a, r, base, slices, st);   // NVFP4 only (layer_slice_ok)
+      return d->fmt == FTMOE_NVFP4 ? layer_slice_launch<FTMOE_NVFP4, 1>(a, r, base, slices, st)
+                                   : layer_slice_launch<FTMOE_MXFP4, 1>(a, r, base, slices, st);
     }
     return d->fmt == FTMOE_NVFP4 ? layer_fused_launch<FTMOE_NVFP4>(a, r, base, st)
                                  : layer_fused_launch<FTMOE_MXFP4>(a, r, base, st);

@@ -99,9 +99,8 @@ def test_layer_path_choice_on_the_host(L):
     weights, separate steps otherwise, -1 for invalid arguments (host logic only)."""
     dec = ft.desc(128, 8, 2048, 768, ft.NVFP4)
     w = _fake_weights(ft.NVFP4, 128, 2048, 768, True)
-    assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), 1) == 2     # one token: the slice form
-    for T in range(2, 9):
-        assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), T) == 1, T
+    for T in range(1, 9):                                                        # the slice form (NVFP4)
+        assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), T) == 2, T
     assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), 9) == 0
     assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), 8192) == 0
     wn = _fake_weights(ft.NVFP4, 128, 2048, 768, False)
@@ -109,6 +108,10 @@ def test_layer_path_choice_on_the_host(L):
     stack = ft.desc(256, 6, 4096, 2048, ft.MXFP4)
     ws = _fake_weights(ft.MXFP4, 225, 4096, 2048, True)
     assert L.ftmoe_layer_path(ctypes.byref(stack), ctypes.byref(ws), 1) == 1   # d 4096: no slice layout
+    small = ft.desc(32, 6, 512, 256, ft.MXFP4)
+    wsm = _fake_weights(ft.MXFP4, 32, 512, 256, True)
+    assert L.ftmoe_layer_path(ctypes.byref(small), ctypes.byref(wsm), 1) == 2   # MXFP4: slice form for one token
+    assert L.ftmoe_layer_path(ctypes.byref(small), ctypes.byref(wsm), 2) == 1   # and the merge form beyond
     fp8 = ft.desc(256, 6, 4096, 2048, ft.FP8_B128)
     w8 = _fake_weights(ft.FP8_B128, 256, 4096, 2048, True)
     assert L.ftmoe_layer_path(ctypes.byref(fp8), ctypes.byref(w8), 1) == 0       # no 4-bit decode layout

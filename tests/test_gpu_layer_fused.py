@@ -1,6 +1,6 @@
 """ftmoe_layer_forward with few tokens and a 4-bit format runs router, sort, expert
-FFN and merge in one kernel (ftmoe_layer_path 1), or, for one token, the slice form
-that applies the down projection per gate/up item (path 2).  Path 1 repeats the
+FFN and merge in one kernel (ftmoe_layer_path 1), or the slice form that applies the
+down projection per gate/up item (path 2: d <= 2048, one token or NVFP4).  Path 1 repeats the
 separate calls' arithmetic (route -> permute -> expert_ffn -> combine) and must equal
 them bit for bit; path 2 regroups the down projection's sums (fp32 reassociation,
 within 1e-5 of the separate calls).  Both match the oracle within the layer's
@@ -42,6 +42,10 @@ def _layer(dsc, W, slot, x, wr, bias, ws=None, want_bf16=True):
         ws = ft.workspace(ft.layer_workspace_size(dsc, T))
     ft.layer_forward(dsc, ft.weights_struct(W), slot, x, wr, bias, ids, w, of, ob, ws)
     return ids, w, of, ob
+
+
+def _expected_path(fmt, d, T):
+    return 2 if d <= 2048 and (T == 1 or fmt == synth.NVFP4) else 1
 
 
 def _same(path, a, b):
@@ -86,7 +90,7 @@ def test_fused_layer_matches_separate_calls_and_oracle(fmt, E, k, d, f, T, renor
         slot_np = np.arange(E, dtype=np.int32)[::-1].copy()
     slot = torch.from_numpy(slot_np).cuda()
     path = ft.layer_path(dsc, ft.weights_struct(W), T)
-    assert path == (2 if T == 1 and d <= 2048 else 1)
+    assert path == _expected_path(fmt, d, T)
     ids, w, of, ob = _layer(dsc, W, slot, x, wr, bias)
     ids_s, w_s, of_s, ob_s = _separate(dsc, W, slot, x, wr, bias)
     assert torch.equal(ids, ids_s)
@@ -117,6 +121,8 @@ def test_skipped_experts_and_a_token_with_none_resident():
     slot_np = np.arange(E, dtype=np.int32)
     slot_np[ids0[0]] = -1
     slot = torch.from_numpy(slot_np).cuda()
+    path = ft.layer_path(dsc, ft.weights_struct(W), T)
+    assert path == _expected_path(fmt, d, T)
     ids, w, of, ob = _layer(dsc, W, slot, x, wr, None)
     ref = OF.layer(weights_to_numpy(W.to("cpu")), slot_np, bf16_bits(x.cpu()), bf16_bits(wr.cpu()), None, k, 1)
     assert np.array_equal(ids.cpu().numpy(), ref["ids"])
@@ -124,7 +130,7 @@ def test_skipped_experts_and_a_token_with_none_resident():
     assert torch.count_nonzero(ob[0].float()).item() == 0
     assert rel_l2(of.cpu().numpy(), ref["out"]) < TOL
     _, _, of_s, _ = _separate(dsc, W, slot, x, wr, None)
-    assert torch.equal(of, of_s)
+    assert _same(path, of, of_s)
     # the two halves of an exact split merge to the full output
     slot_b = np.where(slot_np < 0, np.arange(E), -1).astype(np.int32)
     _, _, of_b, _ = _layer(dsc, W, torch.from_numpy(slot_b).cuda(), x, wr, None)
@@ -145,9 +151,10 @@ def test_repeated_calls_share_one_workspace():
         outs = []
         for rep in range(4):
             x = synth.make_x(T, d, 100 + rep, device="cuda")
+            path = ft.layer_path(dsc, ft.weights_struct(W), T)
             ids, w, of, ob = _layer(dsc, W, slot, x, wr, None, ws=ws, want_bf16=(rep % 2 == 0))
             _, _, of_s, _ = _separate(dsc, W, slot, x, wr, None)
-            assert torch.equal(of, of_s)
+            assert _same(path, of, of_s)
             outs.append(of)
         assert not torch.equal(outs[0], outs[1])
     assert ft.get_device_error() == 0
@@ -164,7 +171,7 @@ def test_full_decode_layer_shape():
     slot = torch.arange(L.E, dtype=torch.int32, device="cuda")
     for T in (1, 4):
         path = ft.layer_path(dsc, ft.weights_struct(W), T)
-        assert path == (2 if T == 1 else 1)
+        assert path == 2
         x = synth.make_x(T, L.d, 12 + T, device="cuda")
         ids, w, of, ob = _layer(dsc, W, slot, x, wr, bias)
         _, _, of_s, ob_s = _separate(dsc, W, slot, x, wr, bias)
@@ -182,9 +189,9 @@ def test_layer_path_query():
     W = synth.make_experts(L.fmt, 4, L.d, L.f, 1, device="cuda")
     assert ft.layer_path(dsc, ft.weights_struct(W), 1) == 0       # not prepared: separate steps
     ft.prepare_weights(dsc, W)
-    assert ft.layer_path(dsc, ft.weights_struct(W), 1) == 2       # one token: the slice form
-    assert ft.layer_path(dsc, ft.weights_struct(W), 2) == 1
-    assert ft.layer_path(dsc, ft.weights_struct(W), 8) == 1
+    assert ft.layer_path(dsc, ft.weights_struct(W), 1) == 2       # the slice form
+    assert ft.layer_path(dsc, ft.weights_struct(W), 2) == 2
+    assert ft.layer_path(dsc, ft.weights_struct(W), 8) == 2
     assert ft.layer_path(dsc, ft.weights_struct(W), 9) == 0       # more tokens: separate steps
     assert ft.layer_path(dsc, ft.weights_struct(W), 0) == -1
 
