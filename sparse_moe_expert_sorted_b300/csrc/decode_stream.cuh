@@ -1381,10 +1381,13 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
         *s_abort = 1;
       }
       if (!eok) continue;
-      // h by batch-token column (zeros for tokens this expert does not serve)
+      // h by batch-token column (zeros for tokens this expert does not serve; one token: column 0
+      // only, the other columns are never read into a kept result)
       uint16_t* hb = s_h + buf * 128;
-      for (int i = lane; i < 128; i += 32) hb[i] = 0;
-      __syncwarp();
+      if (NCOL == 2) {
+        for (int i = lane; i < 128; i += 32) hb[i] = 0;
+        __syncwarp();
+      }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int tok = (lane >> 4) + 2 * j;
@@ -1493,10 +1496,14 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
     }
     // this lane's token columns 2t, 2t + 1: the expert's combine weight for each (0 if it does not serve it)
     float w0 = 0.f, w1 = 0.f;
-    for (int j = 0; j < n; ++j) {
-      const int pj = s_sp[it.lo + j], tk = pj / a.k;
-      if (tk == 2 * t) w0 = s_wt[pj];
-      if (tk == 2 * t + 1) w1 = s_wt[pj];
+    if (NCOL == 1) {
+      if (t == 0) w0 = s_wt[s_sp[it.lo]];   // the one token's pair with this expert
+    } else {
+      for (int j = 0; j < n; ++j) {
+        const int pj = s_sp[it.lo + j], tk = pj / a.k;
+        if (tk == 2 * t) w0 = s_wt[pj];
+        if (tk == 2 * t + 1) w1 = s_wt[pj];
+      }
     }
     // gate/up partials of item q
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
