@@ -1117,14 +1117,17 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
 
 
 // ---------------------------------------------------------------------------
-// One-token layer call, slice form (sl_layer_kernel).  Each gate/up item (16 rows of h) also
+// Layer call, slice form (sl_layer_kernel): one token, or up to 8 with NVFP4 weights, d <= 2048.
+// Each gate/up item (16 rows of h) also
 // carries the down weights that read those 16 values: W_down[:, 16 n0 .. 16 n0 + 16) for all
 // d rows, one NVFP4 block (half an MXFP4 block) of K per row.  Right after the epilogue warp
 // has made the item's 16 h values, the consumer warps multiply them into the down slice
 // (warp w takes rows [w d/16, (w + 1) d/16)) and keep the CTA's partial output for their
-// rows in registers, across all of the CTA's items.  There is no down phase and no wait on
-// other CTAs' h; one grid sync at the end, then every CTA sums the partials of a block of
-// rows over the CTAs in CTA order (deterministic) and writes out in fp32 and bf16.
+// rows in registers, across all of the CTA's items.  With several tokens the h values go by
+// batch-token column (zeros for tokens the expert does not serve), so one register per (row,
+// token) accumulates across experts.  There is no down phase and no wait on other CTAs' h;
+// one grid sync at the end, then every CTA sums the partials of a block of outputs over the
+// CTAs in CTA order (deterministic) and writes out in fp32 and bf16.
 // The combine weight and the block scale multiply the fp32 MMA result of each slice, so
 // out = sum over experts and slices of w * s * (W_slice h_slice): the combine's sum, regrouped.
 //
