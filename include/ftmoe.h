@@ -318,14 +318,19 @@ ftmoe_status ftmoe_lru_copy_slot_of(const ftmoe_lru* lru, int32_t* dst, void* st
 /* One call: the accesses of (layer, topk_ids [B][k]).  Outputs are per access,
  * in access order.  Size them for min(B*k, E) entries:
  *   hit uint8, slot int32, evicted_key int32 (-1 = none)
- *   counters int64 [2]: the handle's running totals (accesses, misses) after the call */
+ *   counters int64 [2] or NULL: the handle's running totals (accesses, misses) after the call
+ * FTMOE_ERR_INVALID_ARG: NULL handle or output, B or k < 1, B*k above 2^31-1, layer
+ * outside [0, L).  An id outside [0, E) is skipped and sets the device error word
+ * (ftmoe_get_device_error). */
 ftmoe_status ftmoe_slot_lru(ftmoe_lru* lru, int layer, const int32_t* topk_ids, int B, int k,
                             uint8_t* hit, int32_t* slot, int32_t* evicted_key, int64_t* counters,
                             void* stream);
 /* A whole trace int32 [steps][L][B][k] in one launch, steps outer, layers inner.
  * Outputs hold every access of the trace in order; capacity (host) is their length.
- *   counters int64 [2]: running totals (accesses, misses); at most `capacity`
- *   accesses are written.  Needing more sets FTMOE_ERR_DEVICE_CHECK. */
+ *   counters int64 [2] or NULL: running totals (accesses, misses); at most `capacity`
+ *   accesses are written.  Needing more sets the device error word.
+ * FTMOE_ERR_INVALID_ARG as for ftmoe_slot_lru, and for steps < 1, capacity < 0 or
+ * steps*L above 2^31-1. */
 ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* lru, const int32_t* trace, int steps, int B, int k,
                                    uint8_t* hit, int32_t* slot, int32_t* evicted_key, int64_t capacity,
                                    int64_t* counters, void* stream);
@@ -336,7 +341,11 @@ ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* lru, const int32_t* trace, int ste
  *   slot_of    int32 [E] or NULL (every expert resident in slot e)
  *   topk_ids, topk_w  outputs as in ftmoe_route (may be NULL only together)
  *   out_f32    fp32 [T][d] (required);  out_bf16  bf16 [T][d] or NULL
- * Two forms (ftmoe_layer_path tells which one a call takes):
+ * Three forms (ftmoe_layer_path tells which one a call takes):
+ *   2  one kernel in the slice form: form 1's router and selection, then each
+ *      gate/up item also applies its 16 columns of the down projection, and the
+ *      CTAs' partial outputs are summed in CTA order at the end.  The sum of form
+ *      1 regrouped: equal up to fp32 reassociation, and the same from run to run.
  *   1  one kernel, for T <= 8 with NVFP4 or MXFP4 weights and weights->prepared:
  *      every CTA computes the logits of its share of the experts, one grid-wide
  *      sync, then every CTA selects the top-k and sorts the pairs itself and

@@ -797,6 +797,7 @@ ftmoe_status ftmoe_lru_copy_slot_of(const ftmoe_lru* h, int32_t* dst, void* stre
 ftmoe_status ftmoe_slot_lru(ftmoe_lru* h, int layer, const int32_t* ids, int B, int k, uint8_t* hit, int32_t* slot,
                             int32_t* ev, int64_t* counters, void* stream) {
   if (!h || !ids || !hit || !slot || !ev || B < 1 || k < 1) return FTMOE_ERR_INVALID_ARG;
+  if ((long long)B * k > INT32_MAX) return FTMOE_ERR_INVALID_ARG;
   if (layer < 0 || layer >= h->st.L) return FTMOE_ERR_INVALID_ARG;
   const long long cap = std::min<long long>((long long)B * k, h->st.E);
   return launch(lru_kernel, dim3(1), dim3(kLruThreads), lru_smem_bytes(h->st.L, h->st.E, h->st.C),
@@ -807,6 +808,7 @@ ftmoe_status ftmoe_slot_lru(ftmoe_lru* h, int layer, const int32_t* ids, int B, 
 ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* h, const int32_t* trace, int steps, int B, int k, uint8_t* hit,
                                    int32_t* slot, int32_t* ev, int64_t capacity, int64_t* counters, void* stream) {
   if (!h || !trace || !hit || !slot || !ev || steps < 1 || B < 1 || k < 1 || capacity < 0) return FTMOE_ERR_INVALID_ARG;
+  if ((long long)B * k > INT32_MAX || (long long)steps * h->st.L > INT32_MAX) return FTMOE_ERR_INVALID_ARG;
   return launch(lru_kernel, dim3(1), dim3(kLruThreads), lru_smem_bytes(h->st.L, h->st.E, h->st.C),
                 as_stream(stream), h->st, trace, steps * h->st.L, B * k, 0, 1, hit, slot, ev, (long long)capacity,
                 reinterpret_cast<long long*>(counters));

@@ -118,3 +118,164 @@ def test_layer_path_choice_on_the_host(L):
     assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(w), 0) == -1
     wrong = _fake_weights(ft.MXFP4, 128, 2048, 768, True)                       # format differs from the layer
     assert L.ftmoe_layer_path(ctypes.byref(dec), ctypes.byref(wrong), 1) == -1
+
+
+# Fake, 256-byte aligned device addresses: every case below fails a host check before any
+# pointer is dereferenced or any CUDA call is made.
+A = 0x10000
+
+
+def _w(fmt, C=4, d=256, f=512, prepared=False, **over):
+    w = _fake_weights(fmt, C, d, f, prepared)
+    for k, v in over.items():
+        setattr(w, k, v)
+    return w
+
+
+def test_quantize_act_argument_checks(L):
+    d = ft.desc(8, 2, 256, 512, ft.NVFP4)
+    q = L.ftmoe_quantize_act
+    assert q(ctypes.byref(d), A, 0, A, A, None) == 1                 # T < 1
+    assert q(ctypes.byref(d), A, (1 << 20) + 1, A, A, None) == 1     # T above 2^20
+    assert q(ctypes.byref(d), None, 4, A, A, None) == 1
+    assert q(ctypes.byref(d), A + 8, 4, A, A, None) == 1             # x not 16-byte aligned
+    assert q(ctypes.byref(d), A, 4, A + 4, A, None) == 1             # codes not 8-byte aligned
+    assert q(ctypes.byref(d), A, 4, A, None, None) == 1
+    d8 = ft.desc(8, 2, 256, 512, ft.FP8_B128)
+    assert q(ctypes.byref(d8), A, 4, A, A + 2, None) == 1            # fp32 scales not 4-byte aligned
+
+
+def test_combine_argument_checks(L):
+    d = ft.desc(8, 2, 256, 512, ft.BF16)
+    c = L.ftmoe_combine
+    #        desc           T  y  pair_pos w  ids slot_of partial_b out_f32 out_bf16
+    assert c(ctypes.byref(d), 4, A, A, A, A, None, None, None, None, None) == 1       # no output
+    assert c(ctypes.byref(d), 0, A, A, A, A, None, None, A, None, None) == 1          # T < 1
+    assert c(ctypes.byref(d), 4, A, None, A, A, None, None, A, None, None) == 1       # y without pair_pos
+    assert c(ctypes.byref(d), 4, A, A, None, A, None, None, A, None, None) == 1       # y without weights
+    assert c(ctypes.byref(d), 4, A, A, A, None, A, None, A, None, None) == 1          # slot_of without ids
+    assert c(ctypes.byref(d), 4, A + 4, A, A, A, None, None, A, None, None) == 1      # y misaligned
+    assert c(ctypes.byref(d), 4, None, None, None, None, None, A + 4, A, None, None) == 1   # partial_b misaligned
+    assert c(ctypes.byref(d), 4, A, A, A, A, None, None, A + 8, None, None) == 1      # out_f32 misaligned
+    assert c(ctypes.byref(d), 4, A, A, A, A, None, None, None, A + 2, None) == 1      # out_bf16 misaligned
+
+
+def test_prepare_weights_argument_checks(L):
+    dn = ft.desc(8, 2, 256, 512, ft.NVFP4)
+    p = L.ftmoe_prepare_weights
+    need = L.ftmoe_prepare_weights_size(ctypes.byref(dn), 4)
+    assert need > 0
+    assert p(ctypes.byref(dn), None, A, need, None) == 1
+    assert p(ctypes.byref(dn), ctypes.byref(_w(ft.MXFP4)), A, need, None) == 1          # format differs
+    assert p(ctypes.byref(dn), ctypes.byref(_w(ft.NVFP4, d=512)), A, need, None) == 1   # d differs
+    assert p(ctypes.byref(dn), ctypes.byref(_w(ft.NVFP4, tensor_scale=None)), A, need, None) == 1
+    assert p(ctypes.byref(dn), ctypes.byref(_w(ft.NVFP4, gate=A + 8)), A, need, None) == 1
+    assert p(ctypes.byref(dn), ctypes.byref(_w(ft.NVFP4)), None, need, None) == 1
+    assert p(ctypes.byref(dn), ctypes.byref(_w(ft.NVFP4)), A + 8, need, None) == 1
+    assert p(ctypes.byref(dn), ctypes.byref(_w(ft.NVFP4)), A, need - 1, None) == 4
+    # BF16 and FP8 need no prepared layout: size 0 and a no-op
+    for fmt in (ft.BF16, ft.FP8_B128):
+        df = ft.desc(8, 2, 256, 512, fmt)
+        assert L.ftmoe_prepare_weights_size(ctypes.byref(df), 4) == 0
+        assert p(ctypes.byref(df), ctypes.byref(_w(fmt)), None, 0, None) == 0
+    assert L.ftmoe_prepare_weights_size(ctypes.byref(dn), 0) == 0
+
+
+def test_prepared_size_grows_with_the_slots(L):
+    for fmt in (ft.NVFP4, ft.MXFP4):
+        d = ft.desc(128, 8, 2048, 768, fmt)
+        one = L.ftmoe_prepare_weights_size(ctypes.byref(d), 1)
+        assert one > 0
+        # each slot's prepared layout is at least as large as its canonical packed weights
+        canonical = 3 * 2048 * 768 // 2
+        assert one >= canonical
+        assert L.ftmoe_prepare_weights_size(ctypes.byref(d), 47) >= 47 * canonical
+
+
+def test_expert_ffn_argument_checks(L):
+    d = ft.desc(8, 2, 256, 512, ft.BF16)
+    f = L.ftmoe_expert_ffn
+    need = L.ftmoe_expert_ffn_workspace_size(ctypes.byref(d), 4)
+    w = ctypes.byref(_w(ft.BF16))
+    #        desc           weights slot_of x  T  off sp topk_w out ws  bytes
+    assert f(ctypes.byref(d), w, None, A, 0, A, A, None, A, A, need, None) == 1
+    assert f(ctypes.byref(d), w, None, A, 4, None, A, None, A, A, need, None) == 1
+    assert f(ctypes.byref(d), w, None, A, 4, A, None, None, A, A, need, None) == 1
+    assert f(ctypes.byref(d), w, None, A, 4, A, A, None, None, A, need, None) == 1
+    assert f(ctypes.byref(d), w, None, A, 4, A, A, None, A + 4, A, need, None) == 1    # out misaligned
+    assert f(ctypes.byref(d), w, None, A + 2, 4, A, A, None, A, A, need, None) == 1    # x misaligned
+    assert f(ctypes.byref(d), w, None, A, 4, A, A, None, A, None, need, None) == 1
+    assert f(ctypes.byref(d), w, None, A, 4, A, A, None, A, A, need - 1, None) == 4
+    assert f(ctypes.byref(d), None, None, A, 4, A, A, None, A, A, need, None) == 1
+
+
+def test_expert_ffn_path_choice(L):
+    path = L.ftmoe_expert_ffn_path
+    for fmt in (ft.BF16, ft.NVFP4, ft.MXFP4, ft.FP8_B128):
+        d = ft.desc(128, 8, 2048, 768, fmt)
+        assert path(ctypes.byref(d), 1) == 0                          # decode: weight-only streaming
+        assert path(ctypes.byref(d), 255) == 0
+    big = {ft.BF16: 0, ft.NVFP4: 1, ft.MXFP4: 0, ft.FP8_B128: 2}
+    for fmt, want in big.items():
+        d = ft.desc(128, 8, 2048, 768, fmt)
+        assert path(ctypes.byref(d), 256) == want
+        assert path(ctypes.byref(d), 8192) == want
+    assert path(ctypes.byref(ft.desc(128, 8, 2048, 768, ft.NVFP4)), 0) == -1
+    assert path(ctypes.byref(ft.desc(128, 8, 2048, 700, ft.NVFP4)), 256) == -1       # ffn % 128 != 0
+
+
+def test_layer_forward_argument_checks(L):
+    d = ft.desc(8, 2, 256, 512, ft.NVFP4)
+    lf = L.ftmoe_layer_forward
+    need = L.ftmoe_layer_workspace_size(ctypes.byref(d), 4)
+    assert need > 0
+    w = ctypes.byref(_w(ft.NVFP4, prepared=True))
+    #          desc          weights slot_of x  w_router bias T ids tw out_f32 out_bf16 ws bytes
+    assert lf(ctypes.byref(d), w, None, A, A, None, 0, A, A, A, None, A, need, None) == 1
+    assert lf(ctypes.byref(d), w, None, A, A, None, 4, A, None, A, None, A, need, None) == 1    # ids without tw
+    assert lf(ctypes.byref(d), w, None, A, A, None, 4, None, A, A, None, A, need, None) == 1    # tw without ids
+    assert lf(ctypes.byref(d), w, None, A, A, None, 4, A, A, None, None, A, need, None) == 1    # no out_f32
+    assert lf(ctypes.byref(d), w, None, A, None, None, 4, A, A, A, None, A, need, None) == 1    # no router
+    assert lf(ctypes.byref(d), w, None, A + 8, A, None, 4, A, A, A, None, A, need, None) == 1
+    assert lf(ctypes.byref(d), w, None, A, A, None, 4, A, A, A, A + 2, A, need, None) == 1     # out_bf16 misaligned
+    assert lf(ctypes.byref(d), ctypes.byref(_w(ft.MXFP4)), None, A, A, None, 4, A, A, A, None, A, need, None) == 1
+    assert lf(ctypes.byref(d), w, None, A, A, None, 4, A, A, A, None, A, need - 1, None) == 4
+    assert lf(ctypes.byref(d), w, None, A, A, None, 4, A, A, A, None, None, need, None) == 1
+
+
+def test_route_noalloc_argument_checks(L):
+    d = ft.desc(128, 8, 2048, 768, ft.NVFP4)
+    r = L.ftmoe_route_noalloc
+    assert r(ctypes.byref(d), A, A, None, 0, A, A, None) == 1
+    assert r(ctypes.byref(d), None, A, None, 4, A, A, None) == 1
+    assert r(ctypes.byref(d), A, A, None, 4, None, A, None) == 1
+    assert r(ctypes.byref(d), A + 8, A, None, 4, A, A, None) == 1
+    # the library's fixed logits array holds FTMOE_NOALLOC_MAX_LOGITS = 262144 entries
+    assert r(ctypes.byref(d), A, A, None, 262144 // 128 + 1, A, A, None) == 4
+
+
+def test_lru_argument_checks(L):
+    s = L.ftmoe_slot_lru
+    assert s(None, 0, A, 4, 2, A, A, A, A, None) == 1
+    assert L.ftmoe_slot_lru_replay(None, A, 4, 1, 2, A, A, A, 16, A, None) == 1
+    assert L.ftmoe_lru_reset(None, None) == 1
+    assert L.ftmoe_lru_destroy(None) == 1
+    assert L.ftmoe_lru_copy_slot_of(None, A, None) == 1
+    assert L.ftmoe_lru_slot_of(None) is None
+    assert L.ftmoe_get_device_error(None, None) == 1
+    for Lyr, E, C in [(0, 8, 4), (1, 0, 4), (1, 8, 0), (-1, 8, 4)]:
+        assert L.ftmoe_lru_create(Lyr, E, C, ctypes.byref(ctypes.c_void_p())) == 1
+    assert L.ftmoe_lru_create(1, 8, 4, None) == 1
+    # the state must fit in shared memory: (L*E + 3C + ceil(E/32)) * 4 bytes <= 200 KiB
+    assert L.ftmoe_lru_create(200, 256, 225, ctypes.byref(ctypes.c_void_p())) == 2
+    assert L.ftmoe_lru_create(1, 32, 17056, ctypes.byref(ctypes.c_void_p())) == 2    # 51201 ints, one too many
+
+
+def test_status_strings_cover_every_code(L):
+    seen = set()
+    for code in range(7):
+        s = L.ftmoe_status_string(code)
+        assert s and s != b"unknown status"
+        seen.add(s)
+    assert len(seen) == 7
+    assert L.ftmoe_status_string(99) == b"unknown status"
