@@ -22,7 +22,8 @@ Modules:
 
 Parity status: every function is pinned by the `-m "not gpu"` tests in
 tests/test_oracle_*.py against closed forms, library routines, brute force
-or hand-derived golden values, except the softmax weights and the SiLU.
-Those two are pinned only by tolerance against fp64 brute force.
+or hand-derived golden values.  The softmax weights are pinned against
+scipy.special.softmax and the two-expert sigmoid; the SiLU against
+scipy.special.expit, sigmoid(ln 3) = 3/4 and silu(g) - silu(-g) = g.
 """
 from . import formats, route, permute, ffn, lru  # noqa: F401

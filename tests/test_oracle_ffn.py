@@ -9,6 +9,7 @@
     (banandre.com, "The 284B Model on a 32GB GPU Trick", section "The q*
     Policy: Math Instead of Guesses").
   * Linearity in the combine weights, slot indirection, and zero-token experts.
+  * SiLU against scipy.special.expit and its closed-form values.
 """
 import math
 
@@ -122,3 +123,37 @@ def test_layer_tokens_matches_whole_layer():
     toks = [0, 5, 15]
     part = O.layer_tokens(W, slot_of, x, res["ids"], res["w"], toks)
     assert rel_l2(part, res["out"][toks]) < 1e-13
+
+
+def test_silu_matches_scipy_expit_and_the_odd_identity():
+    """With X = I, W_gate = diag(g), W_up = I and W_down = I one expert's output is
+    diag(silu(g)).  silu(g) = g * expit(g) (scipy.special.expit, a library routine),
+    silu(0) = 0, and silu(g) - silu(-g) = g for every g.  A transposed operand would
+    move the values off the diagonal."""
+    from scipy.special import expit
+    g = np.array([0.0, 0.5, -0.5, 1.0986122886681098, -3.0, 7.5, -40.0, 30.0])
+    n = g.size
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(n)
+    Wg = np.diag(g)[perm]          # hidden unit j: gate g[perm[j]] on input perm[j]
+    I = np.eye(n)
+    Wu, Wd = I[perm], I[perm].T    # up: input perm[j] -> unit j; down: unit j -> output perm[j]
+    Y = O.swiglu(I, Wg, Wu, Wd)
+    want = np.diag(g * expit(g))
+    assert np.allclose(Y, want, rtol=1e-14, atol=1e-300)
+    assert Y[0, 0] == 0.0
+    # sigmoid(ln 3) = 3/4
+    assert abs(Y[3, 3] - 0.75 * 1.0986122886681098) < 1e-15
+    Yn = O.swiglu(I, -Wg, Wu, Wd)
+    assert np.allclose(np.diag(Y) - np.diag(Yn), g, rtol=0, atol=1e-13)
+
+
+def test_silu_saturates_without_overflow():
+    """Very negative gate values give 0 (exp overflow in the denominator is harmless);
+    very positive ones give the identity."""
+    g = np.array([-800.0, -100.0, 100.0, 800.0])
+    I = np.eye(4)
+    Y = np.diag(O.swiglu(I, np.diag(g), I, I))
+    assert np.all(np.isfinite(Y))
+    assert Y[0] == 0.0 and abs(Y[1]) < 1e-40
+    assert Y[2] == 100.0 and Y[3] == 800.0

@@ -5,7 +5,7 @@ The router logits are pinned in three ways:
   * an error bound against the exact rational dot product;
   * selection that agrees with brute force over all k-subsets.
 The softmax weights are pinned against the closed form sigmoid(l1 - l2) for
-two experts, and against invariants.
+two experts, against scipy.special.softmax, and against invariants.
 """
 import itertools
 import json
@@ -112,3 +112,34 @@ def test_route_invariants_on_random_inputs():
     assert np.all(w > 0) and np.allclose(w.sum(1), 1.0, atol=1e-6)
     _, w0, _ = R.route(x, wr, None, k, renorm=0)
     assert np.all(w0.sum(1) < 1.0)
+
+
+def test_weights_match_scipy_softmax():
+    """The weights against scipy.special.softmax (a library routine, computed from the
+    fp32 logits in fp64): every expert's probability for k = E, and the renormalised
+    share of the chosen experts for k < E."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(11)
+    lg = (rng.standard_normal((6, 12)) * 3.0).astype(np.float32)
+    ids, w = R.select_topk(lg, 12, renorm=0)
+    p = softmax(lg.astype(np.float64), axis=1)
+    for t in range(lg.shape[0]):
+        assert np.allclose(w[t], p[t, ids[t]].astype(np.float32), rtol=2 ** -22, atol=0)
+    ids, w = R.select_topk(lg, 4, renorm=1)
+    for t in range(lg.shape[0]):
+        share = p[t, ids[t]] / p[t, ids[t]].sum()
+        assert np.allclose(w[t], share.astype(np.float32), rtol=2 ** -22, atol=0)
+    ids, w = R.select_topk(lg, 4, renorm=0)
+    for t in range(lg.shape[0]):
+        assert np.allclose(w[t], p[t, ids[t]].astype(np.float32), rtol=2 ** -22, atol=0)
+
+
+def test_weights_are_shift_invariant_and_stable_for_large_logits():
+    """Softmax ignores a common shift of the logits; large logits neither overflow nor
+    lose the winner's share (exp(1000) would overflow without the max shift)."""
+    lg = np.array([[0.0, 1.0, -2.0, 0.5]], np.float32)
+    ids0, w0 = R.select_topk(lg, 2, renorm=0)
+    ids1, w1 = R.select_topk(lg + np.float32(1000.0), 2, renorm=0)
+    assert np.array_equal(ids0, ids1)
+    assert np.all(np.isfinite(w1))
+    assert np.allclose(w0, w1, rtol=1e-4)
