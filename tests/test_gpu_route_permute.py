@@ -9,6 +9,7 @@ the 256x6 stack at batch 1/16/64, prefill chunks) plus edge cases:
   * exact ties;
   * renorm off;
   * an unscaled N(0,1) router;
+  * the largest expert count and top-k (1024, 32);
   * more than one permutation chunk;
   * every pair on one expert.
 """
@@ -65,6 +66,13 @@ def test_route_prefill_paths_with_ragged_tiles(T):
     _check_route(128, 8, 2048, T, seed=T, bias_zero=True)
 
 
+@pytest.mark.parametrize("T,renorm", [(1, 1), (5, 0), (70, 1)])
+def test_route_largest_expert_count_and_top_k(T, renorm):
+    """E = 1024 and k = 32, the largest the descriptor allows: each lane of the selecting
+    warp holds 32 experts and every lane ends up holding one rank."""
+    _check_route(1024, 32, 256, T, seed=40 + T, renorm=renorm)
+
+
 def test_route_renorm_off_unscaled_router_and_k_equals_E():
     _check_route(16, 4, 256, 40, seed=5, renorm=0, scaled=False)
     _check_route(8, 8, 256, 9, seed=6)
@@ -95,7 +103,7 @@ def _check_permute(E, k, ids_np):
 
 @pytest.mark.parametrize("E,k,T", [(8, 2, 16), (8, 2, 1), (128, 8, 1), (128, 8, 16), (256, 6, 64),
                                    (128, 8, 128), (128, 8, 129), (128, 8, 8192), (256, 6, 16384),
-                                   (1024, 4, 3000)])
+                                   (1024, 4, 3000), (1024, 32, 100)])
 def test_permute_matches_oracle(E, k, T):
     g = np.random.default_rng(E * 7 + T)
     ids = np.argsort(g.random((T, E)), axis=1)[:, :k].astype(np.int32)
