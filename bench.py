@@ -476,7 +476,52 @@ def finish(args, ws, wl, L, T, K, ms_max, value, stack, n_layers, eb, roofline, 
         "roofline": roofline, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clk,
     }
     lru.close()
+    if not args.experts:
+        try:
+            res["lru_replay"] = lru_replay(wl, T, stack)
+        except Exception as e:     # the replay is a side report: never lose the bench line over it
+            res["lru_replay"] = {"error": str(e)[:200]}
     return res
+
+
+def lru_replay(wl, T, stack, dev="cuda"):
+    """The workload's routing trace (Gumbel-top-k over the Zipf ranks) replayed through the
+    global LRU in one ftmoe_slot_lru_replay launch from a cold table: access and miss counts,
+    and the device time of the replay (CUDA events, best of 3 cold-start replays)."""
+    import sparse_moe_expert_sorted_b300 as ft
+    if not wl.capacity or not wl.trace_steps:
+        return None
+    L = wl.layer
+    nl = wl.layers if stack else 1
+    trace = synth.make_trace(wl.trace_steps, nl, T, L.k, L.E, wl.zipf_s, seed=wl.seed)
+    steps = trace.shape[0]
+    cap = steps * nl * min(T * L.k, L.E)
+    h = ft.LRU(nl, L.E, wl.capacity)
+    try:
+        tr = torch.from_numpy(np.ascontiguousarray(trace)).to(dev)
+        hit = torch.empty(cap, dtype=torch.uint8, device=dev)
+        slot = torch.empty(cap, dtype=torch.int32, device=dev)
+        ev = torch.empty(cap, dtype=torch.int32, device=dev)
+        cnt = torch.zeros(2, dtype=torch.int64, device=dev)
+        h.replay(tr, hit, slot, ev, cnt)
+        acc, miss = (int(v) for v in cnt.tolist())
+        times = []
+        for _ in range(3):
+            h.reset()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record()
+            h.replay(tr, hit, slot, ev, cnt)
+            t1.record()
+            t1.synchronize()
+            times.append(t0.elapsed_time(t1))
+        again = [int(v) for v in cnt.tolist()]
+    finally:
+        h.close()
+    return {"trace_steps": steps, "layers": nl, "tokens_per_step": T, "experts_per_token": L.k,
+            "capacity": wl.capacity, "accesses": acc, "misses": miss, "miss_rate": round(miss / max(1, acc), 4),
+            "repeatable": again == [acc, miss], "replay_us_per_step": round(min(times) * 1e3 / steps, 3),
+            "how": "one ftmoe_slot_lru_replay launch per replay, cold start; synthetic iid Zipf trace"}
 
 
 def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
