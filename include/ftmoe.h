@@ -234,7 +234,9 @@ ftmoe_status ftmoe_permute(const ftmoe_layer_desc* desc, const int32_t* topk_ids
  *   h = silu(X W_gate^T) * (X W_up^T),   y = h W_down^T
  * where X holds the rows x[p / k] of those pairs.  Experts with slot_of[e] < 0
  * are skipped: that is one side of an exact split.
- *   slot_of   int32 [E]: slot index in `weights`, or -1
+ *   slot_of   int32 [E]: slot index in `weights`, or -1.  An entry >= weights->C
+ *             is a data error: that expert is skipped and the device error word
+ *             is set (code 2)
  *   topk_w    NULL: y_or_out is y, fp32 [P][d] in sorted order (row j = pair
  *             sorted_pair[j]); rows of skipped experts are left untouched
  *             otherwise: fused combine.  y_or_out is out fp32 [T][d], and
@@ -277,7 +279,8 @@ ftmoe_status ftmoe_expert_ffn(const ftmoe_layer_desc* desc, const ftmoe_weights*
  *   out_t = partial_b_t + sum_{r: slot_of[ids[t,r]] >= 0} w[t,r] * y[pair_pos[t*k+r]]
  * summed in ascending r, in fp32.
  *   y          fp32 [P][d] sorted rows, or NULL (then out = partial_b, a cast/merge only)
- *   slot_of    int32 [E] or NULL (= every expert resident)
+ *   slot_of    int32 [E] or NULL (= every expert resident); this call does not know
+ *              the arena, so every entry >= 0 counts as resident
  *   partial_b  fp32 [T][d] or NULL
  *   out_f32    fp32 [T][d] or NULL; out_bf16 bf16 [T][d] or NULL (round to nearest even)
  * ------------------------------------------------------------------------- */
@@ -338,7 +341,8 @@ ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* lru, const int32_t* trace, int ste
 /* ---------------------------------------------------------------------------
  * Whole layer in one call: route -> permute -> expert FFN -> combine -> bf16.
  * This is the same work as the four calls above, on one workspace.
- *   slot_of    int32 [E] or NULL (every expert resident in slot e)
+ *   slot_of    int32 [E] or NULL (every expert resident in slot e); an entry
+ *              >= weights->C is skipped in every step and sets the device error word
  *   topk_ids, topk_w  outputs as in ftmoe_route (may be NULL only together)
  *   out_f32    fp32 [T][d] (required);  out_bf16  bf16 [T][d] or NULL
  * Three forms (ftmoe_layer_path tells which one a call takes):

@@ -14,6 +14,7 @@ namespace ftmoe {
 
 struct CombineArgs {
   int T, k, d, E;
+  int C;                     // slots of the arena: an entry >= C was skipped by the FFN (not resident)
   const float* y;
   const int32_t* pair_pos;
   const float* topk_w;
@@ -42,7 +43,8 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
             set_dev_err(DEV_ERR_BAD_ID);
             continue;
           }
-          if (a.slot_of[e] < 0) continue;
+          const int slot = a.slot_of[e];
+          if (slot < 0 || slot >= a.C) continue;
         }
         const float w = a.topk_w[p];
         const float4 v = reinterpret_cast<const float4*>(a.y + size_t(a.pair_pos[p]) * a.d)[c4];

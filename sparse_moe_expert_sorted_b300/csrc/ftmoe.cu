@@ -573,14 +573,17 @@ ftmoe_status ffn_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, const i
   return FTMOE_ERR_UNSUPPORTED;
 }
 
+// C: the arena's slot count when the caller knows it (the layer call), so that a slot_of
+// entry the FFN skipped as out of range adds nothing here either; INT32_MAX otherwise.
 ftmoe_status combine_impl(const ftmoe_layer_desc* d, int T, const float* y, const int32_t* pp, const float* w,
                           const int32_t* ids, const int32_t* slot_of, const float* pb, float* of, uint16_t* ob,
-                          cudaStream_t st) {
+                          cudaStream_t st, int C = INT32_MAX) {
   CombineArgs a;
   a.T = T;
   a.k = d->k;
   a.d = d->d;
   a.E = d->E;
+  a.C = C;
   a.y = y;
   a.pair_pos = pp;
   a.topk_w = w;
@@ -979,7 +982,7 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
     s = ffn_path(d, T) == 1 ? ffn_tc_impl(d, w, slot_of, x, T, off, sp, w_, out_f32, view, out_f32, st)
                             : ffn_tc8_impl(d, w, slot_of, x, T, off, sp, w_, out_f32, view, out_f32, st);
     if (s != FTMOE_OK || !out_bf16) return s;
-    return combine_impl(d, T, nullptr, pp, w_, ids_, slot_of, out_f32, out_f32, out_bf16, st);
+    return combine_impl(d, T, nullptr, pp, w_, ids_, slot_of, out_f32, out_f32, out_bf16, st, w->C);
   }
   if (ffn_dec_kernel(d, T) && out_bf16) {
     // decode kernel: fused combine into out_f32, which it zeroes first and casts to bf16 last
@@ -987,7 +990,7 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
   }
   s = ffn_impl(d, w, slot_of, x, T, off, sp, nullptr, y, view, base, st);
   if (s != FTMOE_OK) return s;
-  return combine_impl(d, T, y, pp, w_, ids_, slot_of, nullptr, out_f32, out_bf16, st);
+  return combine_impl(d, T, y, pp, w_, ids_, slot_of, nullptr, out_f32, out_bf16, st, w->C);
 }
 
 }  // extern "C"
