@@ -106,3 +106,30 @@ def test_replay_stack_workload_trace(B):
     assert np.array_equal(h, oh) and np.array_equal(sl, os_) and np.array_equal(ev, oe)
     assert cnt.tolist() == [o.n_access, o.n_miss]
     assert np.array_equal(slot_of, o.slot_of)
+
+
+def test_replay_output_capacity_is_checked_on_the_device():
+    """Output buffers shorter than the trace's accesses: the first `capacity` accesses are
+    written, the running counts still cover the whole trace, and the device error word
+    reads 3 (output capacity); nothing is written past the buffers."""
+    L, E, C, B, k, steps = 1, 16, 5, 2, 2, 50
+    trace = synth.make_trace(steps, L, B, k, E, 1.1, seed=3)
+    o = GlobalLRU(L, E, C)
+    oh, os_, oe = o.replay(trace)
+    cap = len(oh) // 2
+    lru = ft.LRU(L, E, C)
+    guard = 64
+    hit = torch.full((cap + guard,), 7, dtype=torch.uint8, device="cuda")
+    slot = torch.full((cap + guard,), -9, dtype=torch.int32, device="cuda")
+    ev = torch.full((cap + guard,), -9, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(2, dtype=torch.int64, device="cuda")
+    ft.get_device_error()                                   # clear
+    lru.replay(torch.from_numpy(np.ascontiguousarray(trace)).cuda(), hit[:cap], slot[:cap], ev[:cap], cnt)
+    assert ft.get_device_error() == 3
+    assert np.array_equal(hit[:cap].cpu().numpy(), oh[:cap])
+    assert np.array_equal(slot[:cap].cpu().numpy(), os_[:cap])
+    assert np.array_equal(ev[:cap].cpu().numpy(), oe[:cap])
+    assert (hit[cap:] == 7).all() and (slot[cap:] == -9).all() and (ev[cap:] == -9).all()
+    assert cnt.cpu().tolist() == [o.n_access, o.n_miss]
+    assert np.array_equal(lru.slot_of().cpu().numpy(), o.slot_of)
+    lru.close()
