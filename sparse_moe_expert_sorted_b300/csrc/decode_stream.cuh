@@ -834,17 +834,17 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
         const float* rb = s_red + buf * Ls.nred;
         if (phase == 0) {
           // h = silu(gate) * up for the item's 16 rows and n tokens, stored as f16.  Lane: row
-          // lane & 15, tokens (lane >> 4) + 2q.
+          // lane & 15, tokens (lane >> 4) + 2j.
           float gs[4], us[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int row = lane & 15, tok = (lane >> 4) + 2 * q;
-            gs[q] = us[q] = 0.f;
+          for (int j = 0; j < 4; ++j) {
+            const int row = lane & 15, tok = (lane >> 4) + 2 * j;
+            gs[j] = us[j] = 0.f;
             if (tok < n) {
 #pragma unroll 4
               for (int w = 0; w < kSdCons; ++w) {
-                gs[q] += rb[((w * 2 + 0) * 16 + row) * xr + tok];
-                us[q] += rb[((w * 2 + 1) * 16 + row) * xr + tok];
+                gs[j] += rb[((w * 2 + 0) * 16 + row) * xr + tok];
+                us[j] += rb[((w * 2 + 1) * 16 + row) * xr + tok];
               }
             }
           }
@@ -852,10 +852,10 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
           if (lane == 0) mbar_arrive(red_empty + 8 * buf);   // the buffer is free again
           const float tsg = s_ts[3 * it.e + 0], tsu = s_ts[3 * it.e + 1];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int row = lane & 15, tok = (lane >> 4) + 2 * q;
+          for (int j = 0; j < 4; ++j) {
+            const int row = lane & 15, tok = (lane >> 4) + 2 * j;
             if (tok < n) {
-              const float gg = gs[q] * tsg, uu = us[q] * tsu;
+              const float gg = gs[j] * tsg, uu = us[j] * tsu;
               const float h = __fdividef(gg, 1.f + __expf(-gg)) * uu;
               if (!isfinite(h)) set_dev_err(DEV_ERR_NONFINITE);
               h16[size_t(it.lo + p0 + tok) * a.f + it.n0 * kSdRowsA + row] = __half_as_ushort(__float2half_rn(h));
