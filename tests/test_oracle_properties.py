@@ -3,7 +3,8 @@ cases in test_oracle_route / test_oracle_permute / test_oracle_lru, over drawn s
 seeds and tie patterns.
   * selection: the chosen set maximises the summed logit, ties broken toward the
     lexicographically smallest ids (brute force over every k-subset), ordered by
-    (logit desc, id asc); weights positive and summing to 1 with renorm;
+    (logit desc, id asc); weights non-negative, non-increasing along the ranks, and
+    summing to 1 with renorm;
   * permutation: the O(P*E) scan;
   * LRU: Mattson's stack-distance rule and a move-to-front list.
 """
@@ -20,7 +21,7 @@ from oracle.permute import permute
 from test_oracle_lru import _keys_of_trace, move_to_front, stack_distance_hits
 from test_oracle_permute import brute_force
 
-SETTINGS = settings(max_examples=40, deadline=None)
+SETTINGS = settings(max_examples=40, deadline=None, derandomize=True)   # the same draws every run
 
 
 @SETTINGS
@@ -38,7 +39,7 @@ def test_selection_is_the_best_subset(E, data, seed, levels, renorm):
         assert sorted(ids[t].tolist()) == sorted(best)
         order = sorted(best, key=lambda e: (-float(lg[t, e]), e))
         assert ids[t].tolist() == order
-        assert np.all(w[t] > 0)
+        assert np.all(w[t] >= 0) and np.all(np.diff(w[t]) <= 0)   # tiny probabilities may round to 0
         if renorm:
             assert abs(float(w[t].astype(np.float64).sum()) - 1.0) < 1e-6
 
