@@ -110,8 +110,8 @@ typedef struct {
 /* ---------------------------------------------------------------------------
  * ftmoe_prepare_weights - derived layouts of a slot arena that the fast kernels
  * read.  Run once per arena (or after slots are refilled), outside any timed
- * region.  The canonical arena stays the interchange format.  Two parts, in this
- * order in prep:
+ * region.  The canonical arena stays the interchange format.  Up to three parts,
+ * in this order in prep:
  *   1. Prefill (NVFP4, d and ffn multiples of 256): the weight block scales
  *      repacked for the tensor-core path.  Each MMA with K = 64 reads four scales
  *      per row from tensor memory; per 128 weight rows and per K = 64 step the
@@ -131,6 +131,13 @@ typedef struct {
  *      scales][up scales] (R = 16), a down tile [codes][scales] (R = 32).  Its
  *      size equals the canonical bytes of the slot.  Without it (weights->prepared
  *      NULL) the decode path reads the canonical arena, more slowly.
+ *   3. Down slices (NVFP4, MXFP4, d <= 2048), right after part 2: for the layer
+ *      call's slice form, per slot and per 16 columns n0 of W_down (ffn/16
+ *      slices of 9*d bytes): the codes of W_down[:, 16 n0 .. 16 n0 + 16) as
+ *      [d/16 row tiles][32 lanes][4 bytes], lane (g, t) holding bytes 2t and
+ *      2t + 1 of rows g and g + 8 of the tile (the fragment a warp-level MMA
+ *      reads), then one scale byte per row [d] (the block scale covering those 16
+ *      columns).
  * weights->prepared is ignored here.  prep (device, prep_bytes from
  * ftmoe_prepare_weights_size, 256-byte aligned) is written; it is then passed as
  * weights->prepared.  BF16 and FP8_B128 need nothing: size 0, and the call
