@@ -835,7 +835,8 @@ FusedWs fused_ws(const ftmoe_layer_desc* d, int T) {
   F.logits = o; o += align256(size_t(T) * d->E * 4);
   F.ready = o; o += align256(size_t(d->E) * 4);
   F.merge = o; o += align256(size_t(T) * (d->d / 32) * 4);
-  F.part = o; o += align256(size_t(num_sms()) * T * d->d * 4);   // slice form: each CTA's partial output
+  F.part = o;                                                     // slice form: each CTA's partial output
+  if (sl_wanted(d->d, d->fmt)) o += align256(size_t(num_sms()) * T * d->d * 4);
   F.total = o;
   return F;
 }
@@ -886,7 +887,9 @@ LayerWs layer_ws(const ftmoe_layer_desc* d, int T) {
   const size_t sr = route_ws(d, T, true) - kWsHeader;
   const size_t sq = permute_ws(d, T) - kWsHeader;
   const size_t sf = ffn_ws(d, T) - kWsHeader;
-  o += std::max(std::max(sr, sq), std::max(sf, fused_ws(d, T).total));
+  // the one-kernel forms' scratch only where one of them can run (few tokens, 4-bit weights)
+  const bool fusable = T <= kSdRouteMaxT && ffn_path(d, T) == 0 && (d->fmt == FTMOE_NVFP4 || d->fmt == FTMOE_MXFP4);
+  o += std::max(std::max(sr, sq), std::max(sf, fusable ? fused_ws(d, T).total : size_t(0)));
   L.total = o;
   return L;
 }
