@@ -279,3 +279,17 @@ def test_status_strings_cover_every_code(L):
         seen.add(s)
     assert len(seen) == 7
     assert L.ftmoe_status_string(99) == b"unknown status"
+
+
+def test_layer_workspace_holds_only_what_the_call_can_use(L):
+    """The one-kernel forms' scratch (the slice form keeps one partial output per SM) is
+    reserved only where those forms can run: a few tokens with 4-bit weights."""
+    dec = ft.desc(128, 8, 2048, 768, ft.NVFP4)
+    ffn = L.ftmoe_expert_ffn_workspace_size
+    lay = L.ftmoe_layer_workspace_size
+    assert lay(ctypes.byref(dec), 1) >= 148 * 2048 * 4                 # one fp32 partial per SM
+    assert lay(ctypes.byref(dec), 8192) < ffn(ctypes.byref(dec), 8192) + (8 << 20)   # prefill: FFN scratch + pairs
+    fp8 = ft.desc(256, 6, 4096, 2048, ft.FP8_B128)
+    assert lay(ctypes.byref(fp8), 16384) < ffn(ctypes.byref(fp8), 16384) + (8 << 20)
+    stack = ft.desc(256, 6, 4096, 2048, ft.MXFP4)                      # d 4096: no slice form
+    assert lay(ctypes.byref(stack), 1) < 148 * 4096 * 4
