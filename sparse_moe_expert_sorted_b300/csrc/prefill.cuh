@@ -316,6 +316,9 @@ struct GemmCfg {
   static_assert(N % 16 == 0 && N <= 256, "MMA N");
   static_assert(N + 48 <= 256, "accumulator + scale columns must fit 256 TMEM columns");
   static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1024-byte aligned stage buffers");
+  static_assert(SMEM <= 232448, "one CTA's opt-in shared memory");
+  static_assert(STAGE_TX < (1 << 20), "an mbarrier's transaction count");
+  static_assert(OFF_BAR % 8 == 0, "8-byte aligned mbarriers");
 };
 
 template <int MODE, int NH>

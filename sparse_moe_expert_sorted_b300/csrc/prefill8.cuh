@@ -144,6 +144,9 @@ struct G8Cfg {
   static constexpr int STG_BYTES = MODE == 1 ? kEpiWarps * 32 * STG_W * 4 : 0;
   static constexpr int SMEM = OFF_STG + STG_BYTES + 1024;
   static constexpr uint32_t IDESC = idesc_f8(kTileM, N);
+  static_assert(SMEM <= 232448, "one CTA's opt-in shared memory");
+  static_assert(STAGE_TX < (1 << 20), "an mbarrier's transaction count");
+  static_assert(OFF_BAR % 8 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "aligned barriers and stages");
 };
 
 // Epilogue-only barrier: named barrier 2 over the 8 epilogue warps.
