@@ -253,7 +253,9 @@ ftmoe_status ftmoe_permute(const ftmoe_layer_desc* desc, const int32_t* topk_ids
  *      weights the decoded weights meet x and h rounded to f16 in warp-level
  *      MMAs with fp32 accumulation; BF16 and FP8 weights run on CUDA cores in
  *      fp32.  Small T (decode), and every format the tensor-core path does not
- *      cover.
+ *      cover.  A call on this path takes at most (T*k/8 + E) * max(d, ffn) <= 2^28
+ *      work items (a 16384-token chunk at d 4096, top-6: 5.1e7); larger calls
+ *      return FTMOE_ERR_UNSUPPORTED and are split by tokens.
  *   1  NVFP4 weights, T >= FTMOE_PREFILL_MIN_T, d % 256 == 0, ffn % 256 == 0:
  *      tcgen05 block-scaled tensor cores.  The gathered rows of x and h are
  *      quantised to NVFP4 by the rule of ftmoe_quantize_act.  Needs
@@ -364,7 +366,8 @@ ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* lru, const int32_t* trace, int ste
  *      ascending rank, as ftmoe_combine computes it, so the results equal the
  *      separate calls' bit for bit.
  *   0  the separate steps on one stream (the expert FFN with fused combine on
- *      the decode path, the combine call otherwise).
+ *      the decode path, the combine call otherwise), with the expert FFN's size
+ *      limit on its path 0.
  * ------------------------------------------------------------------------- */
 size_t ftmoe_layer_workspace_size(const ftmoe_layer_desc* desc, int T);
 /* Which form ftmoe_layer_forward takes for these weights and T: 0 = separate steps,

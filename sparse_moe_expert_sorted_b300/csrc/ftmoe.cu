@@ -103,6 +103,14 @@ int ffn_path(const ftmoe_layer_desc* d, int T) {
     return 2;
   return 0;
 }
+// The streaming kernels of path 0 index their work items (8-token groups x rows) in 32-bit
+// arithmetic, scaled by the grid in places.  A call stays far inside that range when the worst
+// case, (pairs / 8 + E) groups times the wider matrix dimension, is at most 2^28 (a 16384-token
+// chunk at d 4096 and top-6 needs 5.1e7); larger calls are refused, to be split by tokens.
+bool path0_size_ok(const ftmoe_layer_desc* d, int T) {
+  const long long groups = ((long long)T * d->k + 7) / 8 + d->E;
+  return groups * std::max(d->d, d->ffn) <= (1ll << 28);
+}
 // N tile of the gate/up GEMM: NH gate rows + NH up rows
 int gate_up_nh(const ftmoe_layer_desc* d) { return d->ffn % 96 == 0 ? 96 : 64; }
 
@@ -724,6 +732,7 @@ ftmoe_status ftmoe_expert_ffn(const ftmoe_layer_desc* d, const ftmoe_weights* w,
                               float* y_or_out, void* ws, size_t ws_bytes, void* stream) {
   if (!desc_ok(d) || T < 1 || T > kMaxT || !x || !off || !sp || !y_or_out || !ws) return FTMOE_ERR_INVALID_ARG;
   if (!weights_ok(d, w) || !aligned16(x) || !aligned16(y_or_out)) return FTMOE_ERR_INVALID_ARG;
+  if (ffn_path(d, T) == 0 && !path0_size_ok(d, T)) return FTMOE_ERR_UNSUPPORTED;
   if (ws_bytes < ffn_ws(d, T)) return FTMOE_ERR_WORKSPACE;
   return ffn_impl(d, w, slot_of, x, T, off, sp, topk_w, y_or_out, ws, ws, as_stream(stream));
 }
@@ -916,6 +925,7 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
   if ((ids == nullptr) != (tw == nullptr)) return FTMOE_ERR_INVALID_ARG;
   if (!weights_ok(d, w) || !aligned16(x) || !aligned16(wr) || !aligned16(out_f32)) return FTMOE_ERR_INVALID_ARG;
   if (out_bf16 && (reinterpret_cast<uintptr_t>(out_bf16) & 7u)) return FTMOE_ERR_INVALID_ARG;
+  if (ffn_path(d, T) == 0 && !path0_size_ok(d, T)) return FTMOE_ERR_UNSUPPORTED;
   const LayerWs L = layer_ws(d, T);
   if (ws_bytes < L.total) return FTMOE_ERR_WORKSPACE;
   char* base = static_cast<char*>(ws);

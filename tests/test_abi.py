@@ -293,3 +293,17 @@ def test_layer_workspace_holds_only_what_the_call_can_use(L):
     assert lay(ctypes.byref(fp8), 16384) < ffn(ctypes.byref(fp8), 16384) + (8 << 20)
     stack = ft.desc(256, 6, 4096, 2048, ft.MXFP4)                      # d 4096: no slice form
     assert lay(ctypes.byref(stack), 1) < 148 * 4096 * 4
+
+
+def test_streaming_path_refuses_calls_beyond_its_item_range(L):
+    """Path 0 indexes (pairs / 8 + E) x max(d, ffn) work items in 32-bit arithmetic; calls
+    beyond 2^28 of them return FTMOE_ERR_UNSUPPORTED before any launch."""
+    big = ft.desc(1024, 32, 8192, 8192, ft.BF16)
+    T = 1 << 20                                      # (2^25 / 8 + 1024) x 8192 > 2^28
+    assert L.ftmoe_expert_ffn_path(ctypes.byref(big), T) == 0
+    w = ctypes.byref(_w(ft.BF16, C=1024, d=8192, f=8192))
+    assert L.ftmoe_expert_ffn(ctypes.byref(big), w, None, A, T, A, A, None, A, A, 1 << 62, None) == 2
+    assert L.ftmoe_layer_forward(ctypes.byref(big), w, None, A, A, None, T, A, A, A, None, A, 1 << 62, None) == 2
+    mx = ft.desc(256, 6, 4096, 2048, ft.MXFP4)       # MXFP4 streams at every T: up to 87040 tokens here
+    wm = ctypes.byref(_w(ft.MXFP4, C=256, d=4096, f=2048))
+    assert L.ftmoe_expert_ffn(ctypes.byref(mx), wm, None, A, 400000, A, A, None, A, A, 1 << 62, None) == 2
