@@ -1,7 +1,8 @@
 """Python binding of the ftmoe C ABI (include/ftmoe.h).
 
 Argument marshalling only: every step of the layer runs in the CUDA kernels
-of libftmoe.so.  Tensors are torch CUDA tensors (device memory); streams are
+of libftmoe.so.  Each tensor argument is checked for its type and size first,
+since the library sees only its address.  Tensors are torch CUDA tensors (device memory); streams are
 torch CUDA streams.  Nothing here computes the layer: there is no CPU or
 PyTorch fallback.  If the library is missing, every call raises.
 """
@@ -119,6 +120,38 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _need(t, name, dtype=None, count=None, nbytes=None, optional=False):
+    """Check one tensor argument before its pointer crosses the C ABI: the library sees only
+    the address, so a tensor of the wrong type or too small for what the call reads or writes
+    would be read or written past its end.  Raw integer addresses are the caller's to size."""
+    if t is None:
+        if optional:
+            return
+        raise FtmoeError(f"{name} is required")
+    if isinstance(t, int):
+        return
+    if not isinstance(t, torch.Tensor):
+        raise FtmoeError(f"{name}: expected a torch tensor, got {type(t).__name__}")
+    if dtype is not None and t.dtype != dtype:
+        raise FtmoeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if count is not None and t.numel() < count:
+        raise FtmoeError(f"{name}: needs {count} elements, has {t.numel()}")
+    if nbytes is not None and t.numel() * t.element_size() < nbytes:
+        raise FtmoeError(f"{name}: needs {nbytes} bytes, has {t.numel() * t.element_size()}")
+
+
+def _tokens(x, dsc, name="x"):
+    """T of a [T, d] bf16 activation tensor."""
+    if not isinstance(x, torch.Tensor) or x.dim() != 2 or x.shape[1] != dsc.d:
+        raise FtmoeError(f"{name}: expected a [T, {dsc.d}] tensor")
+    _need(x, name, torch.bfloat16)
+    return x.shape[0]
+
+
+def _ws_bytes(ws):
+    return ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 0
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -182,8 +215,12 @@ def prepare_weights(dsc: LayerDesc, W, stream=None):
 
 
 def quantize_act(dsc, x, codes, scales, stream=None):
-    """ftmoe_quantize_act: x [T, d] bf16 -> NVFP4 codes uint8 [T, d/2] + E4M3 scales uint8 [T, d/16]."""
-    T = x.shape[0]
+    """ftmoe_quantize_act: x [T, d] bf16 -> NVFP4 codes uint8 [T, d/2] + E4M3 scales uint8 [T, d/16]
+    (FP8_B128 layers: codes [T, d] + fp32 scales [T, d/128], any tensor type of that many bytes)."""
+    T = _tokens(x, dsc)
+    fp8 = dsc.fmt == FP8_B128
+    _need(codes, "codes", nbytes=T * dsc.d if fp8 else T * dsc.d // 2)
+    _need(scales, "scales", nbytes=T * (dsc.d // 128) * 4 if fp8 else T * dsc.d // 16)
     _check(lib().ftmoe_quantize_act(ctypes.byref(dsc), _ptr(x), T, _ptr(codes), _ptr(scales), _stream(stream)),
            "ftmoe_quantize_act")
 
@@ -192,16 +229,27 @@ def route_workspace_size(dsc: LayerDesc, T: int) -> int:
     return lib().ftmoe_route_workspace_size(ctypes.byref(dsc), T)
 
 
+def _route_args(dsc, x, w_router, bias, ids, w):
+    T = _tokens(x, dsc)
+    _need(w_router, "w_router", torch.bfloat16, dsc.E * dsc.d)
+    _need(bias, "logit_bias", torch.float32, dsc.E, optional=True)
+    _need(ids, "topk_ids", torch.int32, T * dsc.k)
+    _need(w, "topk_w", torch.float32, T * dsc.k)
+    return T
+
+
 def route(dsc, x, w_router, bias, ids, w, logits, ws, stream=None):
-    T = x.shape[0]
+    T = _route_args(dsc, x, w_router, bias, ids, w)
+    _need(logits, "logits", torch.float32, T * dsc.E, optional=True)
+    _need(ws, "ws")
     _check(lib().ftmoe_route(ctypes.byref(dsc), _ptr(x), _ptr(w_router), _ptr(bias), T, _ptr(ids), _ptr(w),
-                             _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)), "ftmoe_route")
+                             _ptr(logits), _ptr(ws), _ws_bytes(ws), _stream(stream)), "ftmoe_route")
 
 
 def route_noalloc(dsc, x, w_router, bias, ids, w, stream=None):
     """ftmoe_route without a workspace: for callers that cannot allocate device memory.
     Calls sharing the library's fixed scratch must not overlap on the GPU."""
-    T = x.shape[0]
+    T = _route_args(dsc, x, w_router, bias, ids, w)
     _check(lib().ftmoe_route_noalloc(ctypes.byref(dsc), _ptr(x), _ptr(w_router), _ptr(bias), T, _ptr(ids), _ptr(w),
                                      _stream(stream)), "ftmoe_route_noalloc")
 
@@ -211,9 +259,16 @@ def permute_workspace_size(dsc: LayerDesc, T: int) -> int:
 
 
 def permute(dsc, ids, offsets, sorted_pair, pair_pos, ws, stream=None):
+    if not isinstance(ids, torch.Tensor) or ids.dim() != 2 or ids.shape[1] != dsc.k:
+        raise FtmoeError(f"topk_ids: expected a [T, {dsc.k}] tensor")
+    _need(ids, "topk_ids", torch.int32)
     T = ids.shape[0]
+    _need(offsets, "expert_offsets", torch.int32, dsc.E + 1)
+    _need(sorted_pair, "sorted_pair", torch.int32, T * dsc.k)
+    _need(pair_pos, "pair_pos", torch.int32, T * dsc.k)
+    _need(ws, "ws")
     _check(lib().ftmoe_permute(ctypes.byref(dsc), _ptr(ids), T, _ptr(offsets), _ptr(sorted_pair), _ptr(pair_pos),
-                               _ptr(ws), ws.numel(), _stream(stream)), "ftmoe_permute")
+                               _ptr(ws), _ws_bytes(ws), _stream(stream)), "ftmoe_permute")
 
 
 def expert_ffn_workspace_size(dsc: LayerDesc, T: int) -> int:
@@ -226,13 +281,29 @@ def expert_ffn_path(dsc: LayerDesc, T: int) -> int:
 
 
 def expert_ffn(dsc, wstruct, slot_of, x, offsets, sorted_pair, topk_w, y_or_out, ws, stream=None):
-    T = x.shape[0]
+    T = _tokens(x, dsc)
+    P = T * dsc.k
+    _need(slot_of, "slot_of", torch.int32, dsc.E, optional=True)
+    _need(offsets, "expert_offsets", torch.int32, dsc.E + 1)
+    _need(sorted_pair, "sorted_pair", torch.int32, P)
+    _need(topk_w, "topk_w", torch.float32, P, optional=True)
+    _need(y_or_out, "y_or_out", torch.float32, (P if topk_w is None else T) * dsc.d)
+    _need(ws, "ws")
     _check(lib().ftmoe_expert_ffn(ctypes.byref(dsc), ctypes.byref(wstruct), _ptr(slot_of), _ptr(x), T,
                                   _ptr(offsets), _ptr(sorted_pair), _ptr(topk_w), _ptr(y_or_out), _ptr(ws),
-                                  ws.numel(), _stream(stream)), "ftmoe_expert_ffn")
+                                  _ws_bytes(ws), _stream(stream)), "ftmoe_expert_ffn")
 
 
 def combine(dsc, T, y, pair_pos, topk_w, topk_ids, slot_of, partial_b, out_f32, out_bf16, stream=None):
+    P = T * dsc.k
+    _need(y, "y", torch.float32, P * dsc.d, optional=True)
+    _need(pair_pos, "pair_pos", torch.int32, P, optional=y is None)
+    _need(topk_w, "topk_w", torch.float32, P, optional=y is None)
+    _need(topk_ids, "topk_ids", torch.int32, P, optional=y is None or slot_of is None)
+    _need(slot_of, "slot_of", torch.int32, dsc.E, optional=True)
+    _need(partial_b, "partial_b", torch.float32, T * dsc.d, optional=True)
+    _need(out_f32, "out_f32", torch.float32, T * dsc.d, optional=True)
+    _need(out_bf16, "out_bf16", torch.bfloat16, T * dsc.d, optional=True)
     _check(lib().ftmoe_combine(ctypes.byref(dsc), T, _ptr(y), _ptr(pair_pos), _ptr(topk_w), _ptr(topk_ids),
                                _ptr(slot_of), _ptr(partial_b), _ptr(out_f32), _ptr(out_bf16), _stream(stream)),
            "ftmoe_combine")
@@ -248,10 +319,18 @@ def layer_path(dsc: LayerDesc, wstruct, T: int) -> int:
 
 
 def layer_forward(dsc, wstruct, slot_of, x, w_router, bias, ids, topk_w, out_f32, out_bf16, ws, stream=None):
-    T = x.shape[0]
+    T = _tokens(x, dsc)
+    _need(slot_of, "slot_of", torch.int32, dsc.E, optional=True)
+    _need(w_router, "w_router", torch.bfloat16, dsc.E * dsc.d)
+    _need(bias, "logit_bias", torch.float32, dsc.E, optional=True)
+    _need(ids, "topk_ids", torch.int32, T * dsc.k, optional=True)
+    _need(topk_w, "topk_w", torch.float32, T * dsc.k, optional=True)
+    _need(out_f32, "out_f32", torch.float32, T * dsc.d)
+    _need(out_bf16, "out_bf16", torch.bfloat16, T * dsc.d, optional=True)
+    _need(ws, "ws")
     _check(lib().ftmoe_layer_forward(ctypes.byref(dsc), ctypes.byref(wstruct), _ptr(slot_of), _ptr(x),
                                      _ptr(w_router), _ptr(bias), T, _ptr(ids), _ptr(topk_w), _ptr(out_f32),
-                                     _ptr(out_bf16), _ptr(ws), ws.numel(), _stream(stream)), "ftmoe_layer_forward")
+                                     _ptr(out_bf16), _ptr(ws), _ws_bytes(ws), _stream(stream)), "ftmoe_layer_forward")
 
 
 def get_device_error(stream=None) -> int:
@@ -282,12 +361,27 @@ class LRU:
         return out
 
     def step(self, layer, ids, hit, slot, evicted, counters, stream=None):
+        if not isinstance(ids, torch.Tensor) or ids.dim() != 2:
+            raise FtmoeError("topk_ids: expected a [B, k] tensor")
+        _need(ids, "topk_ids", torch.int32)
         B, k = ids.shape
+        n = min(B * k, self.E)
+        _need(hit, "hit", torch.uint8, n)
+        _need(slot, "slot", torch.int32, n)
+        _need(evicted, "evicted_key", torch.int32, n)
+        _need(counters, "counters", torch.int64, 2, optional=True)
         _check(lib().ftmoe_slot_lru(self._h, layer, _ptr(ids), B, k, _ptr(hit), _ptr(slot), _ptr(evicted),
                                     _ptr(counters), _stream(stream)), "ftmoe_slot_lru")
 
     def replay(self, trace, hit, slot, evicted, counters, stream=None):
+        if not isinstance(trace, torch.Tensor) or trace.dim() != 4:
+            raise FtmoeError("trace: expected a [steps, L, B, k] tensor")
+        _need(trace, "trace", torch.int32)
         steps, L, B, k = trace.shape
+        _need(hit, "hit", torch.uint8)
+        _need(slot, "slot", torch.int32, hit.numel())
+        _need(evicted, "evicted_key", torch.int32, hit.numel())
+        _need(counters, "counters", torch.int64, 2, optional=True)
         if L != self.L:
             raise FtmoeError("trace layer count differs from the handle's")
         _check(lib().ftmoe_slot_lru_replay(self._h, _ptr(trace), steps, B, k, _ptr(hit), _ptr(slot), _ptr(evicted),
