@@ -182,6 +182,21 @@ class Weights:
     glob: torch.Tensor
 
 
+def _check_arena(W):
+    """The arena's tensors hold C slots of their matrices in W.fmt (C = W.gate.shape[0])."""
+    C, n = W.gate.shape[0], W.d * W.f
+    per = {BF16: 2 * n, NVFP4: n // 2, MXFP4: n // 2, FP8_B128: n}
+    if W.fmt not in per:
+        raise FtmoeError(f"unknown weight format {W.fmt}")
+    for name in ("gate", "up", "down"):
+        _need(getattr(W, name), name, nbytes=C * per[W.fmt])
+    sc = {NVFP4: n // 16, MXFP4: n // 32, FP8_B128: 4 * (n // (128 * 128))}.get(W.fmt)
+    for name in ("gate_s", "up_s", "down_s"):
+        _need(getattr(W, name), name, nbytes=C * sc if sc else None, optional=not sc)
+    if W.fmt == NVFP4:
+        _need(W.glob, "glob", torch.float32, 3 * C)
+
+
 def weights_struct(W, prepared=None) -> WeightsStruct:
     """ftmoe_weights view of an arena with attributes fmt, d, f, gate, up, down,
     gate_s, up_s, down_s, glob (tensor scale [C, 3], NVFP4 only).  `prepared` is
@@ -189,6 +204,7 @@ def weights_struct(W, prepared=None) -> WeightsStruct:
     by default the one prepare_weights attached to W, if any."""
     if prepared is None:
         prepared = getattr(W, "ftmoe_prepared", None)
+    _check_arena(W)
     return WeightsStruct(W.fmt, W.gate.shape[0], W.d, W.f, _ptr(W.gate), _ptr(W.up), _ptr(W.down),
                          _ptr(W.gate_s), _ptr(W.up_s), _ptr(W.down_s), _ptr(W.glob) if W.fmt == NVFP4 else None,
                          _ptr(prepared))

@@ -134,3 +134,21 @@ def test_lru_step_and_replay():
     _passes_checks(lambda: lru.replay(tr, u8(40), i32(40), i32(40), c))
     _fails(lambda: lru.replay(i32(10, 6), u8(40), i32(40), i32(40), c), "trace")
     _fails(lambda: lru.replay(tr, u8(40), i32(39), i32(40), c), "slot")
+
+
+@pytest.mark.parametrize("fmt", [ft.BF16, ft.NVFP4, ft.MXFP4, ft.FP8_B128])
+def test_weights_struct_checks_the_arena(fmt):
+    import synth
+    W = synth.make_experts(fmt, 3, 256, 256, 0)
+    _passes_checks(lambda: ft.weights_struct(W))
+    short = synth.make_experts(fmt, 3, 256, 256, 0)
+    short.up = short.up[:2].contiguous()                  # two slots where the arena has three
+    _fails(lambda: ft.weights_struct(short), "up")
+    if fmt != ft.BF16:
+        short = synth.make_experts(fmt, 3, 256, 256, 0)
+        short.down_s = short.down_s[:2].contiguous()
+        _fails(lambda: ft.weights_struct(short), "down_s")
+    if fmt == ft.NVFP4:
+        short = synth.make_experts(fmt, 3, 256, 256, 0)
+        short.glob = short.glob[:2].contiguous()
+        _fails(lambda: ft.weights_struct(short), "glob")
