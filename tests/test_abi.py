@@ -307,3 +307,27 @@ def test_streaming_path_refuses_calls_beyond_its_item_range(L):
     mx = ft.desc(256, 6, 4096, 2048, ft.MXFP4)       # MXFP4 streams at every T: up to 87040 tokens here
     wm = ctypes.byref(_w(ft.MXFP4, C=256, d=4096, f=2048))
     assert L.ftmoe_expert_ffn(ctypes.byref(mx), wm, None, A, 400000, A, A, None, A, A, 1 << 62, None) == 2
+
+
+def test_size_queries_are_consistent(L):
+    """Host-side size queries over a sweep of layers: the layer workspace covers each step's
+    own workspace; within one form of the call (the same FFN path, up to 8 tokens or more)
+    sizes never shrink as T grows; the tensor-core paths start at FTMOE_PREFILL_MIN_T = 256;
+    the prepared size grows with the slots."""
+    import itertools
+    shapes = [(8, 2, 256, 512), (128, 8, 2048, 768), (256, 6, 4096, 2048), (300, 2, 256, 128), (1024, 32, 512, 256)]
+    for (E, k, d, f), fmt in itertools.product(shapes, [ft.BF16, ft.NVFP4, ft.MXFP4, ft.FP8_B128]):
+        dsc = ctypes.byref(ft.desc(E, k, d, f, fmt))
+        prev = {}
+        for T in (1, 2, 7, 8, 9, 64, 255, 256, 1000, 8192):
+            lay = L.ftmoe_layer_workspace_size(dsc, T)
+            assert lay >= L.ftmoe_route_workspace_size(dsc, T) - 256
+            assert lay >= L.ftmoe_permute_workspace_size(dsc, T)
+            assert lay >= L.ftmoe_expert_ffn_workspace_size(dsc, T)
+            p = L.ftmoe_expert_ffn_path(dsc, T)
+            assert p in (0, 1, 2) and (p == 0 or T >= 256)
+            form = (p, T <= 8)
+            assert lay >= prev.get(form, 0), (E, k, d, f, fmt, T)
+            prev[form] = lay
+        one, two = L.ftmoe_prepare_weights_size(dsc, 1), L.ftmoe_prepare_weights_size(dsc, 2)
+        assert (one == 0) == (fmt in (ft.BF16, ft.FP8_B128)) and two >= 2 * one - 2048
