@@ -2,19 +2,20 @@
  * ftmoe.h - C ABI of the routed mixture-of-experts layer forward on B300 (sm_103a).
  *
  * The layer follows the FreeToken pages' statement of the problem:
- *   - a small router picks a handful of experts per token, e.g. 6 of 256
+ *   - a small router selects a few experts per token, e.g. 6 of 256
  *     (banandre.com, "The 284B Model on a 32GB GPU Trick", section
  *     "Sparsity Is a Lie (But a Useful One)");
  *   - resident experts run on GPU tensor cores from expert slots, with weights
  *     in MXFP4, NVFP4, FP8 or BF16 (zubnet.ai, "FreeToken, Unsloth GGUF ...
  *     consumer hardware");
- *   - partial sums over a split of the selected experts merge exactly once the
+ *   - partial sums over a split of the selected experts add up exactly once the
  *     layer completes (banandre.com, same page, section "The q* Policy: Math
  *     Instead of Guesses");
- *   - a global LRU over all MoE layers, updated on every miss, decides which
- *     experts are resident (asapai.co.kr, "Running 753B GLM-5.2 on a single
- *     workstation GPU", section "Abandoning fixed offloading in favor of
- *     measured bandwidth"; banandre.com, section "Semantic-Aware Caching").
+ *   - a global LRU over all MoE layers, which admits every missed expert,
+ *     decides which experts are resident (asapai.co.kr, "Running 753B GLM-5.2
+ *     on a single workstation GPU", section "Abandoning fixed offloading in
+ *     favor of measured bandwidth"; banandre.com, section "Semantic-Aware
+ *     Caching").
  *
  * Conventions for every call
  *   - Pointers are DEVICE pointers unless a parameter says "host".  The caller
@@ -149,7 +150,7 @@ ftmoe_status ftmoe_prepare_weights(const ftmoe_layer_desc* desc, const ftmoe_wei
 
 /* ---------------------------------------------------------------------------
  * a1  ftmoe_route - router logits, top-k ids and their weights.
- * Pages: a tiny router selects a handful of experts for each token
+ * Pages: a small router selects a few experts for each token
  * (banandre.com, "The 284B Model on a 32GB GPU Trick", section "Sparsity Is a
  * Lie (But a Useful One)").  Reading: softmax over all E logits, then top-k;
  * ties go to the lower id.
@@ -283,7 +284,7 @@ ftmoe_status ftmoe_expert_ffn(const ftmoe_layer_desc* desc, const ftmoe_weights*
 
 /* ---------------------------------------------------------------------------
  * a5  ftmoe_combine - weighted combine and exact merge.
- * Pages: the partial sums over a split of the selected experts merge exactly
+ * Pages: the partial sums over a split of the selected experts add up exactly
  * once the layer completes (banandre.com, section "The q* Policy").
  *   out_t = partial_b_t + sum_{r: slot_of[ids[t,r]] >= 0} w[t,r] * y[pair_pos[t*k+r]]
  * summed in ascending r, in fp32.
@@ -299,8 +300,8 @@ ftmoe_status ftmoe_combine(const ftmoe_layer_desc* desc, int T, const float* y, 
 
 /* ---------------------------------------------------------------------------
  * a6  global LRU slot map over (layer, expert) keys, key = layer*E + e.
- * Pages: in decode the expert cache is a global LRU updated on every miss
- * (asapai.co.kr, "Running 753B GLM-5.2 on a single workstation GPU", section
+ * Pages: in decode the expert cache is a global LRU that admits every missed
+ * expert (asapai.co.kr, "Running 753B GLM-5.2 on a single workstation GPU", section
  * "Abandoning fixed offloading in favor of measured bandwidth").  It spans all
  * MoE layers (banandre.com, section "Semantic-Aware Caching").  It starts
  * cold (banandre.com, section "Elastic Memory").

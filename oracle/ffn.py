@@ -3,8 +3,8 @@
 The pages say each routed expert is a small feed-forward network.  They say
 GPU tensor cores compute the resident experts (zubnet.ai, "FreeToken, Unsloth
 GGUF ... consumer hardware"; banandre.com, "The 284B Model on a 32GB GPU
-Trick", section "Sparsity Is a Lie").  They also say the partial sums over a
-split of the selected experts "merge exactly" once the layer completes (same
+Trick", section "Sparsity Is a Lie").  They also state that the partial sums
+over a split of the selected experts add up to the full output once the layer completes (same
 banandre.com page, section "The q* Policy: Math Instead of Guesses").
 
 Reading, per expert e with weights W_g, W_u [f, d] and W_d [d, f]:

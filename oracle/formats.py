@@ -1,7 +1,7 @@
 """Number formats of the expert weights, and the prefill activation quantiser.
 
-The pages name the weight formats and nothing else: "MXFP4, NVFP4, FP8 and
-BF16 weights" (zubnet.ai, "FreeToken, Unsloth GGUF ... consumer hardware",
+The pages name four weight formats, MXFP4, NVFP4, FP8 and BF16, and no
+layout (zubnet.ai, "FreeToken, Unsloth GGUF ... consumer hardware",
 single section).  The bit layouts below follow the public OCP Microscaling
 (MX) definitions of E2M1, E4M3 and E8M0 and the NVFP4 block layout:
   * NVFP4: E2M1 values, one E4M3 scale per 16 elements, one fp32 scale per tensor.

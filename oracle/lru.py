@@ -1,7 +1,7 @@
 """Global LRU slot map over (layer, expert) keys.
 
 The pages:
-  * in decode the expert cache is one global LRU, updated on every miss
+  * in decode the expert cache is one global LRU that admits every missed expert
     (asapai.co.kr, "Running 753B GLM-5.2 on a single workstation GPU",
     section "Abandoning fixed offloading in favor of measured bandwidth");
   * the LRU is shared by all MoE layers (banandre.com, "The 284B Model on a

@@ -1,7 +1,7 @@
 // a5: weighted combine and exact merge.
 //
-// Pages: the partial sums over a split of the selected experts "merge exactly"
-// once the layer completes (banandre.com, "The 284B Model on a 32GB GPU
+// Pages: the partial sums over a split of the selected experts add up to the
+// full output, with no approximation, once the layer completes (banandre.com, "The 284B Model on a 32GB GPU
 // Trick", section "The q* Policy: Math Instead of Guesses").
 //
 //   out[t][n] = partial_b[t][n] + sum over resident ranks r (ascending) of w[t][r] * y[pair_pos[t*k+r]][n]

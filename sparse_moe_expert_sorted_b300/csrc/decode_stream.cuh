@@ -4,7 +4,7 @@
 //
 // Pages: resident experts are computed on GPU tensor cores from expert slots
 // (zubnet.ai, "FreeToken, Unsloth GGUF ... consumer hardware"); in decode a
-// token touches a handful of experts (banandre.com, "The 284B Model on a 32GB
+// token touches a few experts (banandre.com, "The 284B Model on a 32GB
 // GPU Trick", section "Sparsity Is a Lie"), so a decode layer is a stream of
 // those experts' weights and is bound by HBM bandwidth.
 //

@@ -1,7 +1,7 @@
 // a1: router logits in the fixed fp32 order R, top-k by (logit desc, id asc),
 // softmax weights.
 //
-// Pages: a tiny router picks a handful of experts per token, e.g. 6 of 256
+// Pages: a small router selects a few experts per token, e.g. 6 of 256
 // (banandre.com, "The 284B Model on a 32GB GPU Trick", section "Sparsity Is a
 // Lie (But a Useful One)").
 //
