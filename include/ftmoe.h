@@ -300,8 +300,8 @@ ftmoe_status ftmoe_combine(const ftmoe_layer_desc* desc, int T, const float* y, 
 
 /* ---------------------------------------------------------------------------
  * a6  global LRU slot map over (layer, expert) keys, key = layer*E + e.
- * Pages: in decode the expert cache is a global LRU that admits every missed
- * expert (asapai.co.kr, "Running 753B GLM-5.2 on a single workstation GPU", section
+ * Pages: at decode time one LRU, global over the layers' experts, admits every
+ * missed expert (asapai.co.kr, "Running 753B GLM-5.2 on a single workstation GPU", section
  * "Abandoning fixed offloading in favor of measured bandwidth").  It spans all
  * MoE layers (banandre.com, section "Semantic-Aware Caching").  It starts
  * cold (banandre.com, section "Elastic Memory").

@@ -1,7 +1,7 @@
 """Router: logits, top-k expert choice, and the weights of the chosen experts.
 
-The pages: a small router chooses a few experts for each token, for example
-6 of 256 routed experts per MoE layer (banandre.com, "The 284B Model on a 32GB
+The pages: a small router chooses a few experts for each token, six out of
+256 in their example model (banandre.com, "The 284B Model on a 32GB
 GPU Trick", section "Sparsity Is a Lie (But a Useful One)").  The pages do not
 give the function.  The library's reading is:
   * softmax over all E logits, then top-k;

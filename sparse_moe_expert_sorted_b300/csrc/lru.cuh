@@ -1,7 +1,7 @@
 // a6: global LRU slot map over (layer, expert) keys.
 //
 // Pages:
-//   - in decode, the expert cache is a global LRU that admits every missed expert
+//   - at decode time one global LRU of experts admits every missed expert
 //     (asapai.co.kr, "Running 753B GLM-5.2 on a single workstation GPU",
 //     section "Abandoning fixed offloading in favor of measured bandwidth");
 //   - it spans all MoE layers (banandre.com, "The 284B Model on a 32GB GPU
