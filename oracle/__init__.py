@@ -25,5 +25,12 @@ tests/test_oracle_*.py against closed forms, library routines, brute force
 or hand-derived golden values.  The softmax weights are pinned against
 scipy.special.softmax and the two-expert sigmoid; the SiLU against
 scipy.special.expit, sigmoid(ln 3) = 3/4 and silu(g) - silu(-g) = g.
+The prefill mirror (ffn.swiglu with act_quant, ffn._mirror and the
+formats.quant_act_* / dequant_act_* pairs it uses) is pinned by hand-derived
+examples in tests/golden/mirror_examples.json: one expert with a diagonal gate
+and permutation up/down matrices in NVFP4 and FP8, two scale blocks each,
+checked step by step; planted mistakes (h or x not quantised, g quantised
+instead of h, a transposed operand, a divided or interleaved scale) each
+change the result (tests/test_oracle_mirror.py).
 """
 from . import formats, route, permute, ffn, lru  # noqa: F401
