@@ -82,3 +82,55 @@ class GlobalLRU:
                 V.append(v)
         cat = lambda xs, dt: np.concatenate(xs).astype(dt) if xs else np.zeros(0, dt)
         return cat(H, np.uint8), cat(S, np.int32), cat(V, np.int32)
+
+    # ------------------------------------------------------------------------------
+    # elastic resize at a safe point
+    # ------------------------------------------------------------------------------
+    def recency(self) -> np.ndarray:
+        """Slots of the resident keys, most recently used first."""
+        used = np.flatnonzero(self.key_of >= 0)
+        return used[np.argsort(-self.stamp[used], kind="stable")]
+
+    def resize(self, C_new: int):
+        """Rebuild the slot map under a new capacity C_new, between calls.
+
+        The pages: at scheduler safe points the expert cache is rebuilt under a
+        revised VRAM budget, without reloading the host pool (banandre.com, "The
+        284B Model on a 32GB GPU Trick", section "Elastic Memory: The VRAM Budget
+        Is a Suggestion").
+
+        Reading:
+          * the C_new most recently used keys stay resident, in the same recency
+            order; the others are evicted;
+          * a kept key whose slot is below C_new keeps it; the kept keys in slots
+            >= C_new (ascending) move to the freed slots below C_new (ascending),
+            so the occupied slots stay 0 .. used-1 and a later miss still takes
+            the lowest free slot;
+          * growing keeps every key in its slot; the new slots are free.
+
+        Returns (moves int32 [n_kept, 2] of (old slot, new slot) for every kept key
+        in ascending old slot, evicted keys int64 in recency order)."""
+        if C_new < 1:
+            raise ValueError("capacity must be at least 1")
+        order = self.recency()
+        kept, gone = order[:C_new], order[C_new:]
+        evicted = self.key_of[gone].copy()
+        for key in evicted:
+            self.slot_of[key // self.E, key % self.E] = -1
+        keep = np.zeros(self.C, bool)
+        keep[kept] = True
+        high = [s for s in range(C_new, self.C) if keep[s]]
+        free_low = [s for s in range(min(C_new, self.C)) if not keep[s]]
+        new_slot = {int(s): int(s) for s in kept if s < C_new}
+        for s, t in zip(high, free_low):
+            new_slot[s] = t
+        key_of = np.full(C_new, -1, np.int64)
+        stamp = np.zeros(C_new, np.int64)
+        for s, t in new_slot.items():
+            key_of[t] = self.key_of[s]
+            stamp[t] = self.stamp[s]
+            key = int(self.key_of[s])
+            self.slot_of[key // self.E, key % self.E] = t
+        self.key_of, self.stamp, self.C = key_of, stamp, C_new
+        moves = np.array(sorted(new_slot.items()), np.int32).reshape(-1, 2)
+        return moves, evicted
