@@ -349,6 +349,91 @@ ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* lru, const int32_t* trace, int ste
                                    int64_t* counters, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * The decode-time expert cache around the LRU (the rows after the hot path).
+ * Pages: a missed expert is either copied over the host link into the GPU cache
+ * or computed where its weights are; for a step with m misses the engine fills
+ * q* ~= m * B_P / B_H of them, B_P the measured link (PCIe) bandwidth and B_H the
+ * measured host-memory bandwidth, and the two partial sums merge exactly after
+ * the layer (banandre.com, "The 284B Model on a 32GB GPU Trick", section "The q*
+ * Policy: Math Instead of Guesses").  The host pool is kept in its final layout
+ * in pinned memory, and at scheduler safe points the cache is rebuilt under a
+ * new VRAM budget without reloading that pool (same page, section "Elastic
+ * Memory: The VRAM Budget Is a Suggestion").
+ * Reading: both executors of the split are GPU work.  Executor A computes the
+ * experts resident in the HBM slot arena; executor B computes the others with
+ * their weights streamed straight from the host pool (an ftmoe_weights whose
+ * arrays are pinned host memory the device can address, one slot per
+ * (layer, expert), slot layer*E + e, passed with prepared = NULL so that the
+ * decode path reads it with plain loads).  out = A + B through ftmoe_combine's
+ * partial_b.  Executor B is meant for the decode path (ftmoe_expert_ffn_path 0).
+ * ------------------------------------------------------------------------- */
+
+/* ftmoe_copy_slots - copy whole slots from one arena to another (or within one).
+ * For i < min(*n_pairs, max_pairs) (n_pairs device int32, or NULL = max_pairs):
+ * slot pairs[i][0] of src -> slot pairs[i][1] of dst: codes, scales, tensor
+ * scales and, when both arenas carry one, the prepared layouts (both or neither
+ * must have prepared; FTMOE_ERR_INVALID_ARG otherwise).  Uses:
+ *   - fills: src = the host pool (pinned host memory, read over the host link
+ *     by the kernel, zero-copy), dst = the HBM arena, pairs = (layer*E + e, slot);
+ *   - compaction after ftmoe_lru_resize shrinks: src = dst = the arena, pairs =
+ *     the resize's moves (pairs with equal slots are skipped; the destinations
+ *     of a shrink are never sources, so the copies do not overlap);
+ *   - migration to an arena of another slot count: pairs = the resize's moves.
+ * Pairs outside either arena are skipped and set the device error word.  Two
+ * pairs must not share a destination.  The arenas have the layer's shape and
+ * format. */
+ftmoe_status ftmoe_copy_slots(const ftmoe_layer_desc* desc, const ftmoe_weights* src, const ftmoe_weights* dst,
+                              const int32_t* pairs, const int32_t* n_pairs, int max_pairs, void* stream);
+
+/* q* of the pages for m misses, q* = m * link_gbs / host_gbs (fp64), and the fill
+ * count: q* rounded half up, clamped to [0, m].  -1 for m < 0 or a bandwidth that is
+ * not positive and finite.  Host arithmetic only. */
+double ftmoe_qstar(int m, double link_gbs, double host_gbs);
+int ftmoe_qstar_fill_count(int m, double link_gbs, double host_gbs);
+
+/* ftmoe_miss_split - split the experts of one ftmoe_slot_lru call between the two
+ * executors.  Run right after that call, on the same stream, with its topk_ids
+ * [B][k] and hit flags.  Reads the handle's slot table as the call left it.
+ *   m = the call's misses; n_fill = fill_override if >= 0, else
+ *   ftmoe_qstar_fill_count(m, link_gbs, host_gbs); then, over the call's experts in
+ *   ascending id (its accesses):
+ *     resident after the call (slot >= 0) and a hit   -> A: slot_of_a[e] = slot
+ *     resident, a miss, among the first n_fill such  -> A, and fill_now gets
+ *                                                       (layer*E + e, slot)
+ *     resident, a miss, beyond those                 -> B: slot_of_b[e] = layer*E + e,
+ *                                                       and fill_later gets the pair
+ *     not resident (its slot went to a later miss of the same call) -> B
+ *   slot_of_a, slot_of_b  int32 [E], -1 where the executor skips the expert
+ *   fill_now, fill_later  int32 [min(B*k, E)][2] (pool slot, arena slot)
+ *   counts                int32 [4]: m, fills now, fills later, experts of B
+ * fill_now must land (ftmoe_copy_slots with n_pairs = counts + 1) before A reads
+ * the arena; fill_later (n_pairs = counts + 2) writes only slots that A does not
+ * read, so it may overlap both executors.  E <= 1024 (else FTMOE_ERR_UNSUPPORTED). */
+ftmoe_status ftmoe_miss_split(const ftmoe_lru* lru, int layer, const int32_t* topk_ids, int B, int k,
+                              const uint8_t* hit, double link_gbs, double host_gbs, int fill_override,
+                              int32_t* slot_of_a, int32_t* slot_of_b, int32_t* fill_now, int32_t* fill_later,
+                              int32_t* counts, void* stream);
+
+/* The handle's current slot count. */
+int ftmoe_lru_capacity(const ftmoe_lru* lru);
+
+/* ftmoe_lru_resize - rebuild the slot map under a new capacity C_new, at a safe point
+ * (no call on the handle in flight).  Reading of the pages' elastic rebuild:
+ *   - the C_new most recently used keys stay resident, in the same recency order;
+ *     the others are evicted;
+ *   - a kept key in a slot below C_new keeps it; kept keys in slots >= C_new, in
+ *     ascending slot order, move to the freed slots below C_new in ascending order,
+ *     so the occupied slots stay 0 .. used-1 and later misses take the lowest free
+ *     slot; growing keeps every key where it is;
+ *   - the running totals carry over.
+ *   moves    int32 [min(C_old, C_new)][2] or NULL: (old slot, new slot) of every kept
+ *            key, in ascending old slot (the pairs for ftmoe_copy_slots)
+ *   n_moves  int32 [1] or NULL: the kept keys
+ * Allocates the new device state, runs on `stream`, synchronises it, then frees the
+ * old state.  FTMOE_ERR_UNSUPPORTED if (L*E + 3*C_new) * 4 bytes exceed 200 KiB. */
+ftmoe_status ftmoe_lru_resize(ftmoe_lru* lru, int C_new, int32_t* moves, int32_t* n_moves, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Whole layer in one call: route -> permute -> expert FFN -> combine -> bf16.
  * This is the same work as the four calls above, on one workspace.
  *   slot_of    int32 [E] or NULL (every expert resident in slot e); an entry

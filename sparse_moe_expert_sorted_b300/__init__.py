@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "BF16", "NVFP4", "MXFP4", "FP8_B128", "LayerDesc", "FtmoeError", "lib", "route", "permute", "expert_ffn",
     "combine", "layer_forward", "LRU", "weights_struct", "workspace", "get_device_error", "prepare_weights",
-    "quantize_act",
+    "quantize_act", "copy_slots", "qstar", "qstar_fill_count", "miss_split",
 ]
 
 BF16, NVFP4, MXFP4, FP8_B128 = 0, 1, 2, 3
@@ -33,7 +33,8 @@ EXPORTS = [
     "ftmoe_expert_ffn_workspace_size", "ftmoe_expert_ffn_path", "ftmoe_expert_ffn", "ftmoe_combine", "ftmoe_lru_create", "ftmoe_lru_reset",
     "ftmoe_lru_destroy", "ftmoe_lru_slot_of", "ftmoe_lru_copy_slot_of", "ftmoe_slot_lru", "ftmoe_slot_lru_replay",
     "ftmoe_layer_workspace_size", "ftmoe_layer_path", "ftmoe_layer_forward", "ftmoe_status_string", "ftmoe_get_device_error",
-    "ftmoe_version",
+    "ftmoe_version", "ftmoe_copy_slots", "ftmoe_qstar", "ftmoe_qstar_fill_count", "ftmoe_miss_split",
+    "ftmoe_lru_capacity", "ftmoe_lru_resize",
 ]
 
 
@@ -93,6 +94,13 @@ def lib() -> ctypes.CDLL:
         "ftmoe_status_string": (ctypes.c_char_p, [_I]),
         "ftmoe_get_device_error": (_I, [ctypes.POINTER(_I), _P]),
         "ftmoe_version": (_I, []),
+        "ftmoe_copy_slots": (_I, [_P, _P, _P, _P, _P, _I, _P]),
+        "ftmoe_qstar": (ctypes.c_double, [_I, ctypes.c_double, ctypes.c_double]),
+        "ftmoe_qstar_fill_count": (_I, [_I, ctypes.c_double, ctypes.c_double]),
+        "ftmoe_miss_split": (_I, [_P, _I, _P, _I, _I, _P, ctypes.c_double, ctypes.c_double, _I, _P, _P, _P, _P, _P,
+                                  _P]),
+        "ftmoe_lru_capacity": (_I, [_P]),
+        "ftmoe_lru_resize": (_I, [_P, _I, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -113,8 +121,8 @@ def _ptr(t):
         return None
     if isinstance(t, int):
         return t
-    if not t.is_cuda:
-        raise FtmoeError("ftmoe takes CUDA tensors (device memory)")
+    if not t.is_cuda and not t.is_pinned():
+        raise FtmoeError("ftmoe takes CUDA tensors (device memory) or pinned host tensors the device can address")
     if not t.is_contiguous():
         raise FtmoeError("ftmoe takes contiguous tensors")
     return t.data_ptr()
@@ -222,7 +230,10 @@ def prepare_weights(dsc: LayerDesc, W, stream=None):
     n = prepare_weights_size(dsc, C)
     if n == 0:
         return None
-    buf = torch.empty(n, dtype=torch.uint8, device=W.gate.device)
+    if W.gate.is_cuda:
+        buf = torch.empty(n, dtype=torch.uint8, device=W.gate.device)
+    else:   # a host pool in pinned memory: the prepare kernels write it over the host link
+        buf = torch.empty(n, dtype=torch.uint8, pin_memory=True)
     ws = weights_struct(W, prepared=0)
     _check(lib().ftmoe_prepare_weights(ctypes.byref(dsc), ctypes.byref(ws), _ptr(buf), n, _stream(stream)),
            "ftmoe_prepare_weights")
@@ -403,6 +414,19 @@ class LRU:
         _check(lib().ftmoe_slot_lru_replay(self._h, _ptr(trace), steps, B, k, _ptr(hit), _ptr(slot), _ptr(evicted),
                                            hit.numel(), _ptr(counters), _stream(stream)), "ftmoe_slot_lru_replay")
 
+    @property
+    def capacity(self) -> int:
+        return lib().ftmoe_lru_capacity(self._h)
+
+    def resize(self, C_new, moves=None, n_moves=None, stream=None):
+        """ftmoe_lru_resize: new capacity at a safe point; moves [min(C_old, C_new), 2] int32 and
+        n_moves [1] int32 receive the (old slot, new slot) pairs of the kept keys."""
+        _need(moves, "moves", torch.int32, 2 * min(self.C, C_new), optional=True)
+        _need(n_moves, "n_moves", torch.int32, 1, optional=True)
+        _check(lib().ftmoe_lru_resize(self._h, int(C_new), _ptr(moves), _ptr(n_moves), _stream(stream)),
+               "ftmoe_lru_resize")
+        self.C = int(C_new)
+
     def close(self):
         if getattr(self, "_h", None):
             lib().ftmoe_lru_destroy(self._h)
@@ -413,3 +437,41 @@ class LRU:
             self.close()
         except Exception:
             pass
+
+
+def copy_slots(dsc, src, dst, pairs, n_pairs=None, max_pairs=None, stream=None):
+    """ftmoe_copy_slots: slot pairs[i][0] of the arena `src` -> slot pairs[i][1] of `dst`
+    (WeightsStruct views; the source may be a pinned host pool)."""
+    if max_pairs is None:
+        max_pairs = pairs.numel() // 2 if isinstance(pairs, torch.Tensor) else 0
+    _need(pairs, "pairs", torch.int32, 2 * max_pairs, optional=max_pairs == 0)
+    _need(n_pairs, "n_pairs", torch.int32, 1, optional=True)
+    _check(lib().ftmoe_copy_slots(ctypes.byref(dsc), ctypes.byref(src), ctypes.byref(dst), _ptr(pairs),
+                                  _ptr(n_pairs), int(max_pairs), _stream(stream)), "ftmoe_copy_slots")
+
+
+def qstar(m: int, link_gbs: float, host_gbs: float) -> float:
+    return lib().ftmoe_qstar(int(m), float(link_gbs), float(host_gbs))
+
+
+def qstar_fill_count(m: int, link_gbs: float, host_gbs: float) -> int:
+    return lib().ftmoe_qstar_fill_count(int(m), float(link_gbs), float(host_gbs))
+
+
+def miss_split(lru, layer, ids, hit, link_gbs, host_gbs, fill_override, slot_of_a, slot_of_b, fill_now, fill_later,
+               counts, stream=None):
+    """ftmoe_miss_split right after lru.step(layer, ids, hit, ...) on the same stream."""
+    if not isinstance(ids, torch.Tensor) or ids.dim() != 2:
+        raise FtmoeError("topk_ids: expected a [B, k] tensor")
+    _need(ids, "topk_ids", torch.int32)
+    B, k = ids.shape
+    n = min(B * k, lru.E)
+    _need(hit, "hit", torch.uint8, n)
+    for t, name in ((slot_of_a, "slot_of_a"), (slot_of_b, "slot_of_b")):
+        _need(t, name, torch.int32, lru.E)
+    for t, name in ((fill_now, "fill_now"), (fill_later, "fill_later")):
+        _need(t, name, torch.int32, 2 * n)
+    _need(counts, "counts", torch.int32, 4)
+    _check(lib().ftmoe_miss_split(lru._h, int(layer), _ptr(ids), B, k, _ptr(hit), float(link_gbs), float(host_gbs),
+                                  int(fill_override), _ptr(slot_of_a), _ptr(slot_of_b), _ptr(fill_now),
+                                  _ptr(fill_later), _ptr(counts), _stream(stream)), "ftmoe_miss_split")

@@ -6,6 +6,7 @@
 #include <new>
 
 #include "common.cuh"
+#include "cache.cuh"
 #include "combine.cuh"
 #include "decode.cuh"
 #include "decode_stream.cuh"
@@ -604,6 +605,83 @@ ftmoe_status combine_impl(const ftmoe_layer_desc* d, int T, const float* y, cons
   return launch(combine_kernel, dim3((unsigned)std::min<long long>(cdiv(n, 256), num_sms() * 8)), dim3(256), 0, st, a);
 }
 
+// Device state of an LRU handle for (L, E, C) in one allocation: slot_of [L*E], key, prev and
+// next per slot, meta [4], then the totals (int64 [2]).
+bool lru_alloc(int L, int E, int C, LruState* st, void** mem) {
+  const size_t n_int = size_t(L) * E + 3 * size_t(C) + 4;
+  const size_t bytes = align256(n_int * sizeof(int32_t)) + 2 * sizeof(long long);
+  void* m = nullptr;
+  if (cudaMalloc(&m, bytes) != cudaSuccess) return false;
+  int32_t* p = static_cast<int32_t*>(m);
+  st->slot_of = p;
+  st->key_of = p + size_t(L) * E;
+  st->prv = st->key_of + C;
+  st->nxt = st->prv + C;
+  st->meta = st->nxt + C;
+  st->totals = reinterpret_cast<long long*>(static_cast<char*>(m) + align256(n_int * sizeof(int32_t)));
+  st->L = L;
+  st->E = E;
+  st->C = C;
+  *mem = m;
+  return true;
+}
+
+// Per-slot byte ranges of every array of an arena pair (same layer shape, both arenas in
+// `fmt`), for slot copies.  The prepared layouts are copied part by part (their part
+// offsets depend on each arena's slot count).  Returns the count, or -1 if the prepared
+// buffers are not both present or both absent.
+int slot_regions(const ftmoe_layer_desc* d, const ftmoe_weights* src, const ftmoe_weights* dst, SlotRegion* r) {
+  int n = 0;
+  auto add = [&](const void* s, void* t, size_t ss, size_t ts, size_t bytes) {
+    if (!bytes) return;
+    SlotRegion& R = r[n++];
+    R.src = static_cast<const uint8_t*>(s);
+    R.dst = static_cast<uint8_t*>(t);
+    R.src_stride = ss;
+    R.dst_stride = ts;
+    R.bytes = bytes;
+    R.vec16 = aligned16(s) && aligned16(t) && ss % 16 == 0 && ts % 16 == 0 && bytes % 16 == 0;
+  };
+  const size_t nd = size_t(d->ffn) * d->d;   // elements of one matrix
+  size_t code = 0, scale = 0;
+  switch (d->fmt) {
+    case FTMOE_BF16: code = 2 * nd; break;
+    case FTMOE_NVFP4: code = nd / 2; scale = nd / 16; break;
+    case FTMOE_MXFP4: code = nd / 2; scale = nd / 32; break;
+    case FTMOE_FP8_B128: code = nd; scale = (nd / (128 * 128)) * 4; break;
+  }
+  add(src->gate, const_cast<void*>(dst->gate), code, code, code);
+  add(src->up, const_cast<void*>(dst->up), code, code, code);
+  add(src->down, const_cast<void*>(dst->down), code, code, code);
+  if (scale) {
+    add(src->gate_scale, const_cast<void*>(dst->gate_scale), scale, scale, scale);
+    add(src->up_scale, const_cast<void*>(dst->up_scale), scale, scale, scale);
+    add(src->down_scale, const_cast<void*>(dst->down_scale), scale, scale, scale);
+  }
+  if (d->fmt == FTMOE_NVFP4) add(src->tensor_scale, const_cast<float*>(dst->tensor_scale), 12, 12, 12);
+  const size_t pb = prep_bytes(d, 1);
+  if (!pb) return n;
+  if ((src->prepared == nullptr) != (dst->prepared == nullptr)) return -1;
+  if (!src->prepared) return n;
+  const uint8_t* sp = static_cast<const uint8_t*>(src->prepared);
+  uint8_t* tp = static_cast<uint8_t*>(const_cast<void*>(dst->prepared));
+  const int sC = src->C, tC = dst->C;
+  if (prep_prefill_bytes(d, 1)) {
+    const size_t gu = prep_gate_up_bytes(d, 1), dn = prep_down_bytes(d, 1);
+    add(sp, tp, gu, gu, gu);
+    add(sp + align1k(prep_gate_up_bytes(d, sC)), tp + align1k(prep_gate_up_bytes(d, tC)), dn, dn, dn);
+  }
+  if (prep_decode_bytes(d, 1)) {
+    const size_t db = sd_slot_bytes(d->d, d->ffn, d->fmt);
+    add(sp + prep_decode_offset(d, sC), tp + prep_decode_offset(d, tC), db, db, db);
+    if (prep_slices_bytes(d, 1)) {
+      const size_t sb = sl_slot_bytes(d->d, d->ffn);
+      add(sp + prep_slices_offset(d, sC), tp + prep_slices_offset(d, tC), sb, sb, sb);
+    }
+  }
+  return n;
+}
+
 }  // namespace
 
 // =============================================================================
@@ -751,26 +829,15 @@ ftmoe_status ftmoe_combine(const ftmoe_layer_desc* d, int T, const float* y, con
 // --- LRU ---------------------------------------------------------------------
 ftmoe_status ftmoe_lru_create(int L, int E, int C, ftmoe_lru** out) {
   if (!out || L < 1 || E < 1 || C < 1) return FTMOE_ERR_INVALID_ARG;
+  if ((long long)L * E > INT32_MAX / 2) return FTMOE_ERR_INVALID_ARG;
   if (lru_smem_bytes(L, E, C) > 200 * 1024) return FTMOE_ERR_UNSUPPORTED;
   ftmoe_lru* h = new (std::nothrow) ftmoe_lru();
   if (!h) return FTMOE_ERR_CUDA;
-  const size_t n_int = size_t(L) * E + 3 * size_t(C) + 4;
-  const size_t bytes = align256(n_int * sizeof(int32_t)) + 2 * sizeof(long long);
-  if (cudaMalloc(&h->mem, bytes) != cudaSuccess) {
+  if (!lru_alloc(L, E, C, &h->st, &h->mem)) {
     delete h;
     return FTMOE_ERR_CUDA;
   }
   cudaGetDevice(&h->device);
-  int32_t* p = static_cast<int32_t*>(h->mem);
-  h->st.slot_of = p;
-  h->st.key_of = p + size_t(L) * E;
-  h->st.prv = h->st.key_of + C;
-  h->st.nxt = h->st.prv + C;
-  h->st.meta = h->st.nxt + C;
-  h->st.totals = reinterpret_cast<long long*>(static_cast<char*>(h->mem) + align256(n_int * sizeof(int32_t)));
-  h->st.L = L;
-  h->st.E = E;
-  h->st.C = C;
   ftmoe_status s = ftmoe_lru_reset(h, nullptr);
   if (s == FTMOE_OK && cudaStreamSynchronize(nullptr) != cudaSuccess) s = FTMOE_ERR_CUDA;
   if (s != FTMOE_OK) {
@@ -824,6 +891,94 @@ ftmoe_status ftmoe_slot_lru_replay(ftmoe_lru* h, const int32_t* trace, int steps
   return launch(lru_kernel, dim3(1), dim3(kLruThreads), lru_smem_bytes(h->st.L, h->st.E, h->st.C),
                 as_stream(stream), h->st, trace, steps * h->st.L, B * k, 0, 1, hit, slot, ev, (long long)capacity,
                 reinterpret_cast<long long*>(counters));
+}
+
+// --- expert cache: elastic resize, slot copies, the q* split ---------------------
+int ftmoe_lru_capacity(const ftmoe_lru* h) { return h ? h->st.C : -1; }
+
+ftmoe_status ftmoe_lru_resize(ftmoe_lru* h, int C_new, int32_t* moves, int32_t* n_moves, void* stream) {
+  if (!h || C_new < 1) return FTMOE_ERR_INVALID_ARG;
+  if (lru_smem_bytes(h->st.L, h->st.E, C_new) > 200 * 1024) return FTMOE_ERR_UNSUPPORTED;
+  LruState nw;
+  void* mem = nullptr;
+  if (!lru_alloc(h->st.L, h->st.E, C_new, &nw, &mem)) return FTMOE_ERR_CUDA;
+  int32_t* scratch = nullptr;
+  if (cudaMalloc(&scratch, size_t(h->st.C) * sizeof(int32_t)) != cudaSuccess) {
+    cudaFree(mem);
+    return FTMOE_ERR_CUDA;
+  }
+  cudaStream_t st = as_stream(stream);
+  ftmoe_status s = launch(lru_resize_kernel, dim3(1), dim3(32), 0, st, h->st, nw, scratch, moves, n_moves);
+  if (s == FTMOE_OK && cudaStreamSynchronize(st) != cudaSuccess) s = FTMOE_ERR_CUDA;
+  cudaFree(scratch);
+  if (s != FTMOE_OK) {   // the old state stays in use
+    cudaFree(mem);
+    return s;
+  }
+  cudaFree(h->mem);
+  h->mem = mem;
+  h->st = nw;
+  return FTMOE_OK;
+}
+
+ftmoe_status ftmoe_copy_slots(const ftmoe_layer_desc* d, const ftmoe_weights* src, const ftmoe_weights* dst,
+                              const int32_t* pairs, const int32_t* n_pairs, int max_pairs, void* stream) {
+  if (!desc_ok(d) || !weights_ok(d, src) || !weights_ok(d, dst) || max_pairs < 0) return FTMOE_ERR_INVALID_ARG;
+  if (max_pairs > 0 && !pairs) return FTMOE_ERR_INVALID_ARG;
+  if (max_pairs == 0) return FTMOE_OK;
+  SlotCopyArgs a;
+  memset(&a, 0, sizeof(a));
+  a.nr = slot_regions(d, src, dst, a.r);
+  if (a.nr < 0) return FTMOE_ERR_INVALID_ARG;
+  a.pairs = pairs;
+  a.n_dev = n_pairs;
+  a.n_max = max_pairs;
+  a.src_C = src->C;
+  a.dst_C = dst->C;
+  a.same = src->gate == dst->gate;
+  unsigned long long big = 16;
+  for (int i = 0; i < a.nr; ++i) big = std::max(big, a.r[i].bytes);
+  const int gx = std::max(1, std::min(128, cdiv((long long)(big / 16), 1024)));
+  const int gy = std::max(1, std::min(max_pairs, std::max(1, num_sms() * 16 / gx)));
+  return launch(copy_slots_kernel, dim3(gx, std::min(gy, 65535)), dim3(256), 0, as_stream(stream), a);
+}
+
+double ftmoe_qstar(int m, double link_gbs, double host_gbs) {
+  if (m < 0 || !(link_gbs > 0.0) || !(host_gbs > 0.0) || link_gbs > 1e300 || host_gbs > 1e300) return -1.0;
+  return double(m) * link_gbs / host_gbs;
+}
+
+int ftmoe_qstar_fill_count(int m, double link_gbs, double host_gbs) {
+  const double q = ftmoe_qstar(m, link_gbs, host_gbs);
+  if (q < 0.0) return -1;
+  const double n = floor(q + 0.5);
+  return n < 0.0 ? 0 : (n > double(m) ? m : int(n));
+}
+
+ftmoe_status ftmoe_miss_split(const ftmoe_lru* h, int layer, const int32_t* ids, int B, int k, const uint8_t* hit,
+                              double link_gbs, double host_gbs, int fill_override, int32_t* slot_of_a,
+                              int32_t* slot_of_b, int32_t* fill_now, int32_t* fill_later, int32_t* counts,
+                              void* stream) {
+  if (!h || !ids || !hit || !slot_of_a || !slot_of_b || !fill_now || !fill_later || !counts) return FTMOE_ERR_INVALID_ARG;
+  if (B < 1 || k < 1 || (long long)B * k > INT32_MAX || layer < 0 || layer >= h->st.L) return FTMOE_ERR_INVALID_ARG;
+  if (fill_override < 0 && ftmoe_qstar(0, link_gbs, host_gbs) < 0.0) return FTMOE_ERR_INVALID_ARG;
+  if (h->st.E > 1024) return FTMOE_ERR_UNSUPPORTED;
+  SplitArgs a;
+  a.slot_of = h->st.slot_of;
+  a.ids = ids;
+  a.Bk = B * k;
+  a.E = h->st.E;
+  a.layer = layer;
+  a.hit = hit;
+  a.link = link_gbs;
+  a.host = host_gbs;
+  a.fill_override = fill_override;
+  a.slot_of_a = slot_of_a;
+  a.slot_of_b = slot_of_b;
+  a.fill_now = fill_now;
+  a.fill_later = fill_later;
+  a.counts = counts;
+  return launch(miss_split_kernel, dim3(1), dim3(256), 0, as_stream(stream), a);
 }
 
 // --- whole layer -------------------------------------------------------------

@@ -331,3 +331,39 @@ def test_size_queries_are_consistent(L):
             prev[form] = lay
         one, two = L.ftmoe_prepare_weights_size(dsc, 1), L.ftmoe_prepare_weights_size(dsc, 2)
         assert (one == 0) == (fmt in (ft.BF16, ft.FP8_B128)) and two >= 2 * one - 2048
+
+
+# --- expert cache calls: q*, slot copies, the split, resize (host checks only) -----------
+def test_qstar_host_arithmetic(L):
+    assert abs(L.ftmoe_qstar(8, 52.7, 77.3) - 8 * 52.7 / 77.3) == 0.0
+    assert L.ftmoe_qstar_fill_count(8, 52.7, 77.3) == 5
+    assert L.ftmoe_qstar_fill_count(8, 11.8, 47.5) == 2
+    assert L.ftmoe_qstar_fill_count(1, 1.0, 2.0) == 1          # 0.5 rounds half up
+    assert L.ftmoe_qstar_fill_count(5, 100.0, 1.0) == 5        # clamped to m
+    for bad in [(-1, 1.0, 1.0), (3, 0.0, 1.0), (3, 1.0, 0.0), (3, float("nan"), 1.0), (3, 1.0, float("inf"))]:
+        assert L.ftmoe_qstar(*bad) == -1.0
+        assert L.ftmoe_qstar_fill_count(*bad) == -1
+
+
+def _ws(C, fmt=ft.NVFP4, d=256, f=256, prepared=None):
+    return ft.WeightsStruct(fmt, C, d, f, 16, 16, 16, 16, 16, 16, 16, prepared)
+
+
+def test_copy_slots_checks_its_arguments_on_the_host(L):
+    d = ft.desc(8, 2, 256, 256, ft.NVFP4)
+    src, dst = _ws(8), _ws(4)
+    assert L.ftmoe_copy_slots(ctypes.byref(d), ctypes.byref(src), ctypes.byref(dst), 16, None, 0, None) == 0
+    assert L.ftmoe_copy_slots(ctypes.byref(d), ctypes.byref(src), ctypes.byref(dst), None, None, 3, None) == 1
+    assert L.ftmoe_copy_slots(ctypes.byref(d), ctypes.byref(src), ctypes.byref(dst), 16, None, -1, None) == 1
+    assert L.ftmoe_copy_slots(ctypes.byref(d), None, ctypes.byref(dst), 16, None, 1, None) == 1
+    other = ft.desc(8, 2, 512, 256, ft.NVFP4)                 # arenas of another shape
+    assert L.ftmoe_copy_slots(ctypes.byref(other), ctypes.byref(src), ctypes.byref(dst), 16, None, 1, None) == 1
+    # prepared layouts must be on both sides or on neither
+    assert L.ftmoe_copy_slots(ctypes.byref(d), ctypes.byref(_ws(8, prepared=256)), ctypes.byref(dst), 16, None, 1,
+                              None) == 1
+
+
+def test_miss_split_and_resize_check_their_arguments_on_the_host(L):
+    assert L.ftmoe_miss_split(None, 0, 16, 1, 8, 16, 1.0, 2.0, -1, 16, 16, 16, 16, 16, None) == 1
+    assert L.ftmoe_lru_resize(None, 4, None, None, None) == 1
+    assert L.ftmoe_lru_capacity(None) == -1
