@@ -71,6 +71,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU baseline sample")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (a smaller case of the same kernels, for profiler captures)")
+    ap.add_argument("--prefill-steps", type=int, default=200,
+                    help="timed steps of the 8192-token prefill leg that the default decode run reports beside "
+                         "its headline (0 = skip the leg)")
     return ap.parse_args()
 
 
@@ -631,6 +634,25 @@ def bench_reference(args, rank, ws):
             "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def prefill_leg(args, rank, ws):
+    """The metric's second leg: the 8192-token prefill layer (128 experts top-8, d 2048, ffn 768,
+    NVFP4), timed like the headline (graph replay between CUDA events, max over ranks), with its
+    own FP4 tensor-core roofline, end-to-end figure and CPU baseline."""
+    import copy
+    pa = copy.copy(args)
+    pa.workload, pa.steps, pa.layers, pa.experts = "prefill", args.prefill_steps, 0, 0
+    pa.warmup = max(3, min(args.warmup, 5))
+    r = bench_ours(pa, rank, ws)
+    keys = ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "dtype", "config", "roofline", "e2e",
+            "gpu_launches", "clocks")
+    out = {k: r[k] for k in keys if k in r}
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, threads, sample, _ = oracle_rate("prefill", args.cpu_seconds)
+        out["cpu_baseline"] = {"value": round(rate, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                               "sample": sample}
+    return out
+
+
 def main():
     args = parse()
     if args.steps <= 0:
@@ -642,11 +664,13 @@ def main():
         return
     rank, ws = dist_init()
     res = bench_ours(args, rank, ws)
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, threads, sample, _ = oracle_rate(args.workload, args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(rate, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                               "sample": sample}
+    if args.workload == "decode" and args.prefill_steps > 0 and not args.experts:
+        res["prefill_8k"] = prefill_leg(args, rank, ws)
     if rank == 0:
-        if not args.no_cpu_baseline:
-            rate, threads, sample, _ = oracle_rate(args.workload, args.cpu_seconds)
-            res["cpu_baseline"] = {"value": round(rate, 4), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                   "sample": sample}
         print(json.dumps(res), flush=True)
     if ws > 1:
         import torch.distributed as dist
