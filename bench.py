@@ -71,6 +71,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU baseline sample")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (a smaller case of the same kernels, for profiler captures)")
+    ap.add_argument("--no-cache-legs", action="store_true",
+                    help="skip the expert-cache (fills, q* split) and streamed-prefill reports")
     ap.add_argument("--prefill-steps", type=int, default=200,
                     help="timed steps of the 8192-token prefill leg that the default decode run reports beside "
                          "its headline (0 = skip the leg)")
@@ -438,28 +440,31 @@ def bench_ours(args, rank, ws):
 
 
 def time_layer_calls(ft, dsc, layers, structs, xs, T, L, n_layers, n, ws_l, main):
-    """Mean device time of one ftmoe_layer_forward launch (CUDA events around each call of a
-    captured sequence that cycles the layer copies) and the mean count of distinct experts."""
+    """Mean device time of one ftmoe_layer_forward launch: a captured sequence of n launches
+    that cycles the layer copies, timed by CUDA events before its first and after its last
+    launch on their stream (events between launches would hold each launch back until the
+    previous one has finished, hiding nothing of its launch latency), divided by n; and the
+    mean count of distinct experts."""
     dev = "cuda"
-    sev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
-    eev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
+    ev0 = torch.cuda.Event(enable_timing=True, external=True)
+    ev1 = torch.cuda.Event(enable_timing=True, external=True)
     ids = [torch.empty(T, L.k, dtype=torch.int32, device=dev) for _ in range(n)]
     tw = torch.empty(T, L.k, dtype=torch.float32, device=dev)
     out = torch.empty(T, L.d, dtype=torch.float32, device=dev)
     out_bf = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=main):
+        ev0.record(main)
         for i in range(n):
             l = layers[i % n_layers]
-            sev[i].record(main)
             ft.layer_forward(dsc, structs[i % n_layers], None, xs[i % len(xs)], l.wr, l.bias, ids[i], tw, out, out_bf,
                              ws_l, main)
-            eev[i].record(main)
+        ev1.record(main)
     with torch.cuda.stream(main):
         g.replay()
         g.replay()
     torch.cuda.synchronize()
-    us = float(np.mean([s.elapsed_time(e) for s, e in zip(sev, eev)])) * 1e3
+    us = ev0.elapsed_time(ev1) * 1e3 / n
     uniq = float(np.mean([len(np.unique(t.cpu().numpy())) for t in ids]))
     return us, uniq
 
@@ -528,25 +533,42 @@ def lru_replay(wl, T, stack, dev="cuda"):
 
 
 def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
-    """Same metric through ftmoe_layer_forward with pinned host inputs and outputs."""
+    """Same metric through the public API with pinned host inputs and outputs: per step the
+    host-buffer layer call (ftmoe_layer_forward_host: H2D of x, the layer, D2H of the bf16
+    output), one prepared ctypes call each; the stack workloads copy x once and run the 8
+    layers on it.  Wall clock over the steps, and the host time spent issuing them."""
     dev = "cuda"
     xh = [synth.make_x(T, L.d, 555 + i).pin_memory() for i in range(8)]
     oh = torch.empty(T, L.d, dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
     of = torch.empty(T, L.d, dtype=torch.float32, device=dev)
     ob = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
     ids = torch.empty(T, L.k, dtype=torch.int32, device=dev)
     tw = torch.empty(T, L.k, dtype=torch.float32, device=dev)
-    ws = ft.workspace(ft.layer_workspace_size(dsc, T))
+    if stack:
+        xd = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
+        ws = ft.workspace(ft.layer_workspace_size(dsc, T))
 
-    def step(i):
-        with torch.cuda.stream(main):
-            xd.copy_(xh[i % len(xh)], non_blocking=True)
-            lis = range(n_layers) if stack else [i % n_layers]
-            for li in lis:
+        def step(i):
+            with torch.cuda.stream(main):
+                xd.copy_(xh[i % len(xh)], non_blocking=True)
+                for li in range(n_layers):
+                    l = layers[li]
+                    ft.layer_forward(dsc, structs[li], None, xd, l.wr, l.bias, ids, tw, of, ob, ws, main)
+                oh.copy_(ob, non_blocking=True)
+        how = "per step: pinned H2D of x, ftmoe_layer_forward per layer, D2H of the bf16 output; wall clock"
+    else:
+        ws = ft.workspace(ft.layer_host_workspace_size(dsc, T))
+        calls = {}
+        for i in range(len(xh)):
+            for li in range(n_layers):
                 l = layers[li]
-                ft.layer_forward(dsc, structs[li], None, xd, l.wr, l.bias, ids, tw, of, ob, ws, main)
-            oh.copy_(ob, non_blocking=True)
+                calls[i, li] = ft.LayerHostCall(dsc, structs[li], None, xh[i], l.wr, l.bias, ids, tw, of, oh, ws,
+                                                main)
+
+        def step(i):
+            calls[i % len(xh), i % n_layers]()
+        how = ("per step: one ftmoe_layer_forward_host call (pinned H2D of x, the layer, D2H of the bf16 output), "
+               "arguments packed once; wall clock")
 
     for i in range(5):
         step(i)
@@ -554,11 +576,12 @@ def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
     t0 = time.perf_counter()
     for i in range(steps):
         step(i)
+    t_issue = time.perf_counter() - t0
     main.synchronize()
     dt = time.perf_counter() - t0
     return {"value": round(T * steps / dt, 3), "unit": "tokens/s", "h2d_bytes_per_step": T * L.d * 2,
             "d2h_bytes_per_step": T * L.d * 2, "steps": steps,
-            "how": "per step: pinned H2D of x, ftmoe_layer_forward per layer, D2H of the bf16 output; wall clock"}
+            "host_issue_us_per_step": round(t_issue * 1e6 / steps, 2), "how": how}
 
 
 # ---------------------------------------------------------------------------
@@ -634,6 +657,225 @@ def bench_reference(args, rank, ws):
             "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def link_and_host_bandwidth(dev="cuda"):
+    """The two bandwidths of the q* policy, measured on this machine: B_P, the host link
+    (pinned host -> device copies, 256 MiB, best of 3), and B_H, the host memory (a 1 GiB
+    copy between host buffers by as many threads as the process may use)."""
+    import concurrent.futures as cf
+    n = 256 << 20
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.copy_(h, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        best = max(best, n / (e0.elapsed_time(e1) / 1e3) / 1e9)
+    del h, d
+    m = 1 << 30
+    a = np.ones(m, np.uint8)
+    b = np.empty_like(a)
+    nt = max(1, len(os.sched_getaffinity(0)))
+    parts = np.array_split(np.arange(m), nt)
+    bounds = [(int(p[0]), int(p[-1]) + 1) for p in parts if len(p)]
+
+    def cp(lo_hi):
+        lo, hi = lo_hi
+        np.copyto(b[lo:hi], a[lo:hi])
+
+    host = 0.0
+    with cf.ThreadPoolExecutor(nt) as ex:
+        list(ex.map(cp, bounds))
+        for _ in range(3):
+            t0 = time.perf_counter()
+            list(ex.map(cp, bounds))
+            host = max(host, 2 * m / (time.perf_counter() - t0) / 1e9)   # read + write bytes
+    return round(best, 2), round(host, 2), nt
+
+
+def cache_leg(steps=300, dev="cuda"):
+    """Decode steps with the 37% slot table: the expert pool in pinned host memory, the LRU's
+    misses filled into HBM slots, and the q* split between executor A (HBM slots) and
+    executor B (streaming the other experts from the host pool), merged exactly.  Tokens/s per
+    policy (q* from the measured bandwidths, fill every miss, fill none), miss counts, and the
+    fill kernel's bandwidth against the host link."""
+    import sparse_moe_expert_sorted_b300 as ft
+    wl = synth.DECODE
+    L = wl.layer
+    T, C = 1, wl.capacity
+    dsc = ft.desc(L.E, L.k, L.d, L.f, L.fmt, L.renorm)
+    Wp = synth.make_experts(L.fmt, L.E, L.d, L.f, 4321, device=dev)
+    pin = lambda t: None if t is None else t.cpu().contiguous().pin_memory()
+    pool = synth.ExpertWeights(Wp.fmt, Wp.d, Wp.f, pin(Wp.gate), pin(Wp.up), pin(Wp.down), pin(Wp.gate_s),
+                               pin(Wp.up_s), pin(Wp.down_s), pin(Wp.glob))
+    del Wp
+    ft.prepare_weights(dsc, pool)
+    z = lambda t: None if t is None else torch.zeros((C,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev)
+    arena = synth.ExpertWeights(pool.fmt, pool.d, pool.f, z(pool.gate), z(pool.up), z(pool.down), z(pool.gate_s),
+                                z(pool.up_s), z(pool.down_s), z(pool.glob))
+    ft.prepare_weights(dsc, arena)
+    s_fill, s_pool, s_arena = ft.weights_struct(pool), ft.weights_struct(pool, prepared=0), ft.weights_struct(arena)
+    wr = synth.make_router(L.E, L.d, 4321, device=dev)
+    bias = torch.from_numpy(synth.make_zipf_bias(L.E, wl.zipf_s, 4321)).to(dev)
+    xs = [synth.make_x(T, L.d, 8000 + i, device=dev) for i in range(64)]
+    P, n = T * L.k, min(T * L.k, L.E)
+    ids = torch.empty(T, L.k, dtype=torch.int32, device=dev)
+    tw = torch.empty(T, L.k, dtype=torch.float32, device=dev)
+    off = torch.empty(L.E + 1, dtype=torch.int32, device=dev)
+    sp = torch.empty(P, dtype=torch.int32, device=dev)
+    pp = torch.empty(P, dtype=torch.int32, device=dev)
+    hit = torch.empty(n, dtype=torch.uint8, device=dev)
+    lslot = torch.empty(n, dtype=torch.int32, device=dev)
+    lev = torch.empty(n, dtype=torch.int32, device=dev)
+    sa = torch.empty(L.E, dtype=torch.int32, device=dev)
+    sb = torch.empty(L.E, dtype=torch.int32, device=dev)
+    now = torch.empty(n, 2, dtype=torch.int32, device=dev)
+    later = torch.empty(n, 2, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(4, dtype=torch.int32, device=dev)
+    tot = torch.zeros(4, dtype=torch.int64, device=dev)
+    y_a = torch.empty(P, L.d, dtype=torch.float32, device=dev)
+    out_b = torch.empty(T, L.d, dtype=torch.float32, device=dev)
+    of = torch.empty(T, L.d, dtype=torch.float32, device=dev)
+    ob = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
+    ws_r = ft.workspace(ft.route_workspace_size(dsc, T))
+    ws_p = ft.workspace(ft.permute_workspace_size(dsc, T))
+    ws_a = ft.workspace(ft.expert_ffn_workspace_size(dsc, T))
+    ws_b = ft.workspace(ft.expert_ffn_workspace_size(dsc, T))
+    main, side, fill = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    B_P, B_H, host_threads = link_and_host_bandwidth(dev)
+
+    def run(policy, nsteps):
+        lru = ft.LRU(1, L.E, C)
+        tot.zero_()
+        ev_sel, ev_b, ev_a = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(main):
+            for i in range(nsteps):
+                x = xs[i % len(xs)]
+                ft.route(dsc, x, wr, bias, ids, tw, None, ws_r, main)
+                ft.permute(dsc, ids, off, sp, pp, ws_p, main)
+                lru.step(0, ids, hit, lslot, lev, None, main)
+                override = {"qstar": -1, "fill_all": L.k, "fill_none": 0}[policy]
+                ft.miss_split(lru, 0, ids, hit, B_P, B_H, override, sa, sb, now, later, cnt, main)
+                tot.add_(cnt.to(torch.int64))
+                ev_sel.record(main)
+                side.wait_event(ev_sel)                       # executor B: the other experts from the host pool
+                out_b.zero_()
+                ft.expert_ffn(dsc, s_pool, sb, x, off, sp, tw, out_b, ws_b, side)
+                ev_b.record(side)
+                ft.copy_slots(dsc, s_fill, s_arena, now, cnt[1:2], n, main)   # fills before executor A
+                ft.expert_ffn(dsc, s_arena, sa, x, off, sp, None, y_a, ws_a, main)
+                main.wait_event(ev_b)
+                ft.combine(dsc, T, y_a, pp, tw, ids, sa, out_b, of, ob, main)
+                ft.copy_slots(dsc, s_fill, s_arena, later, cnt[2:3], n, main)  # the deferred fills
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        lru.close()
+        t = tot.tolist()
+        return {"tokens_per_s": round(T * nsteps / dt, 1), "us_per_step": round(dt * 1e6 / nsteps, 2),
+                "misses_per_step": round(t[0] / nsteps, 3), "fills_now_per_step": round(t[1] / nsteps, 3),
+                "fills_later_per_step": round(t[2] / nsteps, 3), "experts_of_B_per_step": round(t[3] / nsteps, 3)}
+
+    res = {}
+    for policy in ("qstar", "fill_all", "fill_none"):
+        run(policy, 20)
+        res[policy] = run(policy, steps)
+    # fill bandwidth: C whole experts from the host pool into the arena, one copy_slots launch
+    pairs = torch.stack([torch.arange(C, dtype=torch.int32), torch.arange(C, dtype=torch.int32)], 1).to(dev)
+    per_slot = sum(t[0].numel() * t.element_size() for t in (pool.gate, pool.up, pool.down, pool.gate_s, pool.up_s,
+                                                             pool.down_s, pool.glob))
+    per_slot += ft.prepare_weights_size(dsc, 1)
+    ft.copy_slots(dsc, s_fill, s_arena, pairs, None, C, main)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    ft.copy_slots(dsc, s_fill, s_arena, pairs, None, C, main)
+    e1.record(main)
+    e1.synchronize()
+    fill_gbs = C * per_slot / (e0.elapsed_time(e1) / 1e3) / 1e9
+    q_mean = res["qstar"]["misses_per_step"]
+    return {"workload": f"decode 128x8 d2048 f768 NVFP4, T={T}, slot table C={C} (37%), expert pool in pinned host "
+                        f"memory, {steps} steps", "link_gbs": B_P, "host_gbs": B_H, "host_threads": host_threads,
+            "qstar_at_mean_misses": round(q_mean * B_P / B_H, 3), "policies": res,
+            "fill": {"gbs": round(fill_gbs, 2), "bytes_per_expert": int(per_slot), "experts": C,
+                     "of_link": round(fill_gbs / B_P, 3),
+                     "how": "one ftmoe_copy_slots launch copying C whole slots (codes, scales, prepared layouts) "
+                            "from pinned host memory, CUDA events"},
+            "how": "per step: route, permute, LRU, q* split, fills now, executor A (HBM slots) and executor B "
+                   "(host pool, side stream), exact merge, deferred fills; wall clock over the steps"}
+
+
+def stream_leg(layers=3, dev="cuda"):
+    """Full-layer double buffering: `layers` prefill layers (128x8, d 2048, f 768, NVFP4) whose
+    experts stream from pinned host memory through two device arenas (layer l+1 copied while
+    layer l computes) against one arena (the copy waits for the compute), at 4096, 8192 and
+    16384 tokens."""
+    import sparse_moe_expert_sorted_b300 as ft
+    wl = synth.PREFILL
+    L = wl.layer
+    dsc = ft.desc(L.E, L.k, L.d, L.f, L.fmt, L.renorm)
+    Wp = synth.make_experts(L.fmt, layers * L.E, L.d, L.f, 5150, device=dev)
+    pin = lambda t: None if t is None else t.cpu().contiguous().pin_memory()
+    pool = synth.ExpertWeights(Wp.fmt, Wp.d, Wp.f, pin(Wp.gate), pin(Wp.up), pin(Wp.down), pin(Wp.gate_s),
+                               pin(Wp.up_s), pin(Wp.down_s), pin(Wp.glob))
+    del Wp
+    torch.cuda.empty_cache()
+    ft.prepare_weights(dsc, pool)
+    z = lambda t: None if t is None else torch.zeros((L.E,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev)
+    arenas = []
+    for _ in range(2):
+        A = synth.ExpertWeights(pool.fmt, pool.d, pool.f, z(pool.gate), z(pool.up), z(pool.down), z(pool.gate_s),
+                                z(pool.up_s), z(pool.down_s), z(pool.glob))
+        ft.prepare_weights(dsc, A)
+        arenas.append(A)
+    structs = [ft.weights_struct(a) for a in arenas]
+    routers = [synth.make_router(L.E, L.d, 5160 + l, device=dev) for l in range(layers)]
+    comp, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    out = {}
+    for T in (4096, 8192, 16384):
+        xs = [synth.make_x(T, L.d, 5170 + l, device=dev) for l in range(layers)]
+        of = [torch.empty(T, L.d, device=dev) for _ in range(layers)]
+        ws = ft.workspace(ft.layer_workspace_size(dsc, T))
+        row = {}
+        for n_arenas in (2, 1):
+            times = []
+            for rep in range(4):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(comp)
+                ft.layers_streamed(dsc, ft.weights_struct(pool), structs[:n_arenas], xs, routers, None, of, None, ws,
+                                   stream=comp, copy_stream=copy)
+                e1.record(comp)
+                e1.synchronize()
+                if rep:
+                    times.append(e0.elapsed_time(e1))
+            row[n_arenas] = min(times)
+        # the compute alone: the same layers with their experts already resident
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for rep in range(2):
+            e0.record(comp)
+            for l in range(layers):
+                ft.layer_forward(dsc, structs[0], None, xs[l], routers[l], None, None, None, of[l], None, ws, comp)
+            e1.record(comp)
+            e1.synchronize()
+        compute_ms = e0.elapsed_time(e1)
+        out[str(T)] = {"ms_two_arenas": round(row[2], 3), "ms_one_arena": round(row[1], 3),
+                       "compute_only_ms": round(compute_ms, 3),
+                       "tokens_per_s_two_arenas": round(T * layers / (row[2] / 1e3), 1),
+                       "penalty_without_second_arena": round(1.0 - row[2] / row[1], 4)}
+        del xs, of, ws
+    per_layer = sum(t[:L.E].numel() * t.element_size() for t in (pool.gate, pool.up, pool.down, pool.gate_s,
+                                                                  pool.up_s, pool.down_s, pool.glob))
+    nh = 96 if L.f % 96 == 0 else 64     # the prefill part of the prepared layout (include/ftmoe.h)
+    per_layer += L.E * (L.f // nh) * (L.d // 64) * ((2 * nh + 127) // 128) * 512 + L.E * (L.d // 128) * (L.f // 64) * 512
+    return {"workload": f"{layers} prefill layers 128x8 d2048 f768 NVFP4, experts in pinned host memory, "
+                        "two device arenas vs one", "per_T": out, "bytes_copied_per_layer": int(per_layer),
+            "how": "ftmoe_layers_streamed, CUDA events on the compute stream, best of 3 after one warm-up"}
+
+
 def prefill_leg(args, rank, ws):
     """The metric's second leg: the 8192-token prefill layer (128 experts top-8, d 2048, ffn 768,
     NVFP4), timed like the headline (graph replay between CUDA events, max over ranks), with its
@@ -670,6 +912,13 @@ def main():
                                "sample": sample}
     if args.workload == "decode" and args.prefill_steps > 0 and not args.experts:
         res["prefill_8k"] = prefill_leg(args, rank, ws)
+    if args.workload == "decode" and not args.experts and not args.no_cache_legs:
+        for key, fn in (("cache", cache_leg), ("stream", stream_leg)):
+            try:
+                res[key] = fn()
+            except Exception as e:   # side reports: never lose the headline line over them
+                res[key] = {"error": str(e)[:300]}
+            torch.cuda.empty_cache()
     if rank == 0:
         print(json.dumps(res), flush=True)
     if ws > 1:

@@ -188,8 +188,9 @@ ftmoe_status ftmoe_route(const ftmoe_layer_desc* desc, const uint16_t* x, const 
  * routine.
  *   - T * E must not exceed FTMOE_NOALLOC_MAX_LOGITS (1 MiB of logits); larger
  *     requests return FTMOE_ERR_WORKSPACE.
- *   - The first call on a device looks up the array's device address.  Make that
- *     first call before capturing a stream.
+ *   - The first call on a device looks up the array's device address (and the first
+ *     call after a device reset, which ends the context the address belonged to).  Make
+ *     that first call before capturing a stream.
  *   - All calls share the one array: calls that can overlap on the GPU (other
  *     streams, other host threads) race and must be serialised by the caller.
  * ------------------------------------------------------------------------- */
@@ -433,6 +434,35 @@ int ftmoe_lru_capacity(const ftmoe_lru* lru);
  * old state.  FTMOE_ERR_UNSUPPORTED if (L*E + 3*C_new) * 4 bytes exceed 200 KiB. */
 ftmoe_status ftmoe_lru_resize(ftmoe_lru* lru, int C_new, int32_t* moves, int32_t* n_moves, void* stream);
 
+/* ftmoe_layers_streamed - L MoE layers whose experts stream from a host pool larger than
+ * the device arenas (prefill of a model that does not fit in the GPU's expert budget).
+ * Pages: during prefill, full-layer double buffering streams layer l+1's experts while the
+ * GPU computes layer l, and turning the second buffer off costs throughput that grows with
+ * the prompt length (asapai.co.kr, "Running 753B GLM-5.2 on a single workstation GPU",
+ * section "Abandoning fixed offloading in favor of measured bandwidth"; banandre.com, "The
+ * 284B Model on a 32GB GPU Trick", section "Semantic-Aware Caching").
+ *   pool       the host pool: C >= L*E slots, expert e of layer l in slot l*E + e (pinned
+ *              host memory the device can address); it carries a prepared layout when
+ *              the arenas do
+ *   arenas     n_arenas (1 or 2) device arenas of at least E slots, same format
+ *   x          [L] inputs [T][d] bf16 (device); x[l] == NULL for l > 0 takes out_bf16[l-1]
+ *   w_router   [L] router weights [E][d];  logit_bias [L] or NULL (entries may be NULL)
+ *   out_f32    [L] outputs [T][d] fp32;  out_bf16 [L] or NULL (bf16 outputs)
+ *   ws         the layer call's workspace for T (ftmoe_layer_workspace_size)
+ * For each layer, one cudaMemcpyAsync per array copies its E experts (a contiguous range
+ * of each pool array) into arena l % n_arenas on copy_stream: the canonical arrays and the
+ * part of the prepared layout that the call's path reads.  The layer then runs
+ * (ftmoe_layer_forward, every expert resident) on compute_stream once its copy has landed.
+ * With two arenas the copy of layer l+1 overlaps the compute of layer l; with one it waits
+ * for it.  The copy stream first waits for the work already queued on the compute stream,
+ * and the compute stream's last layer comes after every copy; the two streams must differ.
+ * Asynchronous on both streams. */
+ftmoe_status ftmoe_layers_streamed(const ftmoe_layer_desc* desc, int L, const ftmoe_weights* pool,
+                                   const ftmoe_weights* arenas, int n_arenas, const uint16_t* const* x,
+                                   const uint16_t* const* w_router, const float* const* logit_bias, int T,
+                                   float* const* out_f32, uint16_t* const* out_bf16, void* ws, size_t ws_bytes,
+                                   void* compute_stream, void* copy_stream);
+
 /* ---------------------------------------------------------------------------
  * Whole layer in one call: route -> permute -> expert FFN -> combine -> bf16.
  * This is the same work as the four calls above, on one workspace.
@@ -468,6 +498,20 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* desc, const ftmoe_weigh
                                  const float* logit_bias, int T, int32_t* topk_ids, float* topk_w,
                                  float* out_f32, uint16_t* out_bf16, void* ws, size_t ws_bytes,
                                  void* stream);
+
+/* ftmoe_layer_forward_host - the layer call from and to host memory, for callers whose
+ * activations live on the host.  On `stream`: x_host [T][d] bf16 (host, pinned for an
+ * asynchronous copy) is copied into the workspace, ftmoe_layer_forward runs on it, and
+ * the bf16 output is copied back to out_host [T][d] (host).  topk_ids / topk_w and
+ * out_f32 stay on the device as in ftmoe_layer_forward (out_f32 required).  The
+ * workspace (ftmoe_layer_host_workspace_size) is the layer call's plus staging for x
+ * and the bf16 output.  Asynchronous: out_host is valid once the stream reaches the
+ * end of the call. */
+size_t ftmoe_layer_host_workspace_size(const ftmoe_layer_desc* desc, int T);
+ftmoe_status ftmoe_layer_forward_host(const ftmoe_layer_desc* desc, const ftmoe_weights* weights,
+                                      const int32_t* slot_of, const uint16_t* x_host, const uint16_t* w_router,
+                                      const float* logit_bias, int T, int32_t* topk_ids, float* topk_w,
+                                      float* out_f32, uint16_t* out_host, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Helpers

@@ -17,7 +17,7 @@ import torch
 __all__ = [
     "BF16", "NVFP4", "MXFP4", "FP8_B128", "LayerDesc", "FtmoeError", "lib", "route", "permute", "expert_ffn",
     "combine", "layer_forward", "LRU", "weights_struct", "workspace", "get_device_error", "prepare_weights",
-    "quantize_act", "copy_slots", "qstar", "qstar_fill_count", "miss_split",
+    "quantize_act", "copy_slots", "qstar", "qstar_fill_count", "miss_split", "LayerHostCall", "layers_streamed",
 ]
 
 BF16, NVFP4, MXFP4, FP8_B128 = 0, 1, 2, 3
@@ -34,7 +34,8 @@ EXPORTS = [
     "ftmoe_lru_destroy", "ftmoe_lru_slot_of", "ftmoe_lru_copy_slot_of", "ftmoe_slot_lru", "ftmoe_slot_lru_replay",
     "ftmoe_layer_workspace_size", "ftmoe_layer_path", "ftmoe_layer_forward", "ftmoe_status_string", "ftmoe_get_device_error",
     "ftmoe_version", "ftmoe_copy_slots", "ftmoe_qstar", "ftmoe_qstar_fill_count", "ftmoe_miss_split",
-    "ftmoe_lru_capacity", "ftmoe_lru_resize",
+    "ftmoe_lru_capacity", "ftmoe_lru_resize", "ftmoe_layer_host_workspace_size", "ftmoe_layer_forward_host",
+    "ftmoe_layers_streamed",
 ]
 
 
@@ -101,6 +102,9 @@ def lib() -> ctypes.CDLL:
                                   _P]),
         "ftmoe_lru_capacity": (_I, [_P]),
         "ftmoe_lru_resize": (_I, [_P, _I, _P, _P, _P]),
+        "ftmoe_layer_host_workspace_size": (_SZ, [_P, _I]),
+        "ftmoe_layer_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+        "ftmoe_layers_streamed": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -475,3 +479,72 @@ def miss_split(lru, layer, ids, hit, link_gbs, host_gbs, fill_override, slot_of_
     _check(lib().ftmoe_miss_split(lru._h, int(layer), _ptr(ids), B, k, _ptr(hit), float(link_gbs), float(host_gbs),
                                   int(fill_override), _ptr(slot_of_a), _ptr(slot_of_b), _ptr(fill_now),
                                   _ptr(fill_later), _ptr(counts), _stream(stream)), "ftmoe_miss_split")
+
+
+def layer_host_workspace_size(dsc: LayerDesc, T: int) -> int:
+    return lib().ftmoe_layer_host_workspace_size(ctypes.byref(dsc), T)
+
+
+class LayerHostCall:
+    """ftmoe_layer_forward_host bound once to a set of buffers: x_host and out_host are pinned
+    host tensors [T, d] bf16; everything else is device memory.  The arguments are checked and
+    packed here, once, so that each call is one ctypes call (the per-step cost of a serving loop)."""
+
+    def __init__(self, dsc, wstruct, slot_of, x_host, w_router, bias, ids, topk_w, out_f32, out_host, ws,
+                 stream=None):
+        for t, name in ((x_host, "x_host"), (out_host, "out_host")):
+            if not isinstance(t, torch.Tensor) or t.is_cuda or t.dim() != 2 or t.shape[1] != dsc.d:
+                raise FtmoeError(f"{name}: expected a host [T, {dsc.d}] tensor")
+            _need(t, name, torch.bfloat16)
+        T = x_host.shape[0]
+        if out_host.shape[0] < T:
+            raise FtmoeError("out_host: fewer rows than x_host")
+        _need(slot_of, "slot_of", torch.int32, dsc.E, optional=True)
+        _need(w_router, "w_router", torch.bfloat16, dsc.E * dsc.d)
+        _need(bias, "logit_bias", torch.float32, dsc.E, optional=True)
+        _need(ids, "topk_ids", torch.int32, T * dsc.k, optional=True)
+        _need(topk_w, "topk_w", torch.float32, T * dsc.k, optional=True)
+        _need(out_f32, "out_f32", torch.float32, T * dsc.d)
+        _need(ws, "ws", nbytes=layer_host_workspace_size(dsc, T))
+        self._keep = (dsc, wstruct, slot_of, x_host, w_router, bias, ids, topk_w, out_f32, out_host, ws)
+        self._fn = lib().ftmoe_layer_forward_host
+        self._args = (ctypes.byref(dsc), ctypes.byref(wstruct), _ptr(slot_of), x_host.data_ptr(), _ptr(w_router),
+                      _ptr(bias), T, _ptr(ids), _ptr(topk_w), _ptr(out_f32), out_host.data_ptr(), _ptr(ws),
+                      _ws_bytes(ws), _stream(stream))
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st:
+            _check(st, "ftmoe_layer_forward_host")
+
+
+def layers_streamed(dsc, pool, arenas, xs, routers, biases, outs_f32, outs_bf16, ws, stream=None, copy_stream=None):
+    """ftmoe_layers_streamed over L = len(routers) layers: `pool` and `arenas` are WeightsStruct
+    views (the pool in pinned host memory, C >= L * E); xs[l] None (l > 0) chains the previous
+    layer's bf16 output.  Returns nothing; outputs land in outs_f32 / outs_bf16."""
+    L = len(routers)
+    if not (len(xs) == len(outs_f32) == L) or (outs_bf16 is not None and len(outs_bf16) != L):
+        raise FtmoeError("one input, router and output per layer")
+    if xs[0] is None:
+        raise FtmoeError("the first layer needs an input")
+    T = _tokens(xs[0], dsc)
+    for l in range(L):
+        if xs[l] is not None and _tokens(xs[l], dsc) != T:
+            raise FtmoeError("every layer input has T rows")
+        if xs[l] is None and (outs_bf16 is None or outs_bf16[l - 1] is None):
+            raise FtmoeError(f"layer {l} chains the previous bf16 output, which is missing")
+        _need(routers[l], "w_router", torch.bfloat16, dsc.E * dsc.d)
+        if biases is not None:
+            _need(biases[l], "logit_bias", torch.float32, dsc.E, optional=True)
+        _need(outs_f32[l], "out_f32", torch.float32, T * dsc.d)
+        if outs_bf16 is not None:
+            _need(outs_bf16[l], "out_bf16", torch.bfloat16, T * dsc.d, optional=True)
+    _need(ws, "ws", nbytes=layer_workspace_size(dsc, T))
+    arr = (WeightsStruct * len(arenas))(*arenas)
+    vp = lambda ts: (ctypes.c_void_p * L)(*[_ptr(t) for t in ts])
+    if copy_stream is None:
+        raise FtmoeError("layers_streamed needs a copy stream")
+    _check(lib().ftmoe_layers_streamed(ctypes.byref(dsc), L, ctypes.byref(pool), arr, len(arenas), vp(xs), vp(routers),
+                                       None if biases is None else vp(biases), T, vp(outs_f32),
+                                       None if outs_bf16 is None else vp(outs_bf16), _ptr(ws), _ws_bytes(ws),
+                                       _stream(stream), _stream(copy_stream)), "ftmoe_layers_streamed")

@@ -495,14 +495,18 @@ __device__ __forceinline__ bool wait_count(const unsigned* v, unsigned target, v
 // router's fixed fp32 order: lane j adds the products of its 8-element chunks j, j + 32, ...
 // in ascending element order, unfused; lanes combine by a xor butterfly 16 .. 1; bias last).
 // Router rows are in shared memory (srow), x is read from global memory.  Consumer warps.
+// cl_logit: 0 = write r.logits (global); else the shared-memory address of s_logit [T][E], and
+// the logit goes to that address in each of the cl_n CTAs of the cluster (lane q to rank q).
 __device__ __forceinline__ void sd_route_logits(const FfnArgs& a, const SdRoute& r, const uint8_t* srow, int ne,
-                                                int cw, int lane) {
+                                                int cw, int lane, int e_first, int e_step, uint32_t cl_logit = 0,
+                                                int cl_n = 0) {
   const int S = a.d >> 8;    // chunks per lane
   for (int item = cw; item < ne * a.T; item += kSdCons) {
     const int i = item / a.T, t = item - i * a.T;
-    const int e = blockIdx.x + i * gridDim.x;
+    const int e = e_first + i * e_step;
     const uint4* wrow = reinterpret_cast<const uint4*>(srow + size_t(i) * a.d * 2);
     const uint4* xr = reinterpret_cast<const uint4*>(a.x + size_t(t) * a.d);
+    const float bias = r.bias ? __ldg(r.bias + e) : 0.f;   // issued beside the x loads
     float acc = 0.f;
     for (int s0 = 0; s0 < S; s0 += 8) {
       uint4 xv[8];
@@ -524,9 +528,62 @@ __device__ __forceinline__ void sd_route_logits(const FfnArgs& a, const SdRoute&
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, off));
-    if (lane == 0) {
-      if (r.bias) acc = __fadd_rn(acc, r.bias[e]);
+    if (r.bias) acc = __fadd_rn(acc, bias);
+    if (cl_logit) {
+      if (lane < cl_n) st_cluster_f32(mapa_shared(cl_logit + 4u * uint32_t(t * a.E + e), uint32_t(lane)), acc);
+    } else if (lane == 0) {
       r.logits[size_t(t) * a.E + e] = acc;
+    }
+  }
+}
+
+// Router logits of the cluster form: this CTA's experts e_first + i (i < ne) for T tokens, in
+// order R (as sd_route_logits), each written into s_logit of every CTA of the cluster.  Warp cw
+// takes experts cw and cw + 16 together: x of the token is loaded once into registers with the
+// two biases, and the two experts' chains run side by side (their arithmetic is unchanged).
+// d <= 2048 (at most 8 chunks per lane).  Consumer warps.
+__device__ __forceinline__ void sl_route_logits_cl(const FfnArgs& a, const SdRoute& r, const uint8_t* srow, int ne,
+                                                   int cw, int lane, int e_first, uint32_t cl_logit, int cl_n) {
+  const int S = a.d >> 8;    // chunks per lane (<= 8)
+  for (int i0 = cw; i0 < ne; i0 += 2 * kSdCons) {
+    const int i1 = i0 + kSdCons;
+    const bool two = i1 < ne;
+    const int e0 = e_first + i0, e1 = e_first + (two ? i1 : i0);
+    const uint4* w0 = reinterpret_cast<const uint4*>(srow + size_t(i0) * a.d * 2);
+    const uint4* w1 = reinterpret_cast<const uint4*>(srow + size_t(two ? i1 : i0) * a.d * 2);
+    for (int t = 0; t < a.T; ++t) {
+      const uint4* xr = reinterpret_cast<const uint4*>(a.x + size_t(t) * a.d);
+      uint4 xv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) xv[q] = q < S ? __ldg(xr + q * 32 + lane) : make_uint4(0, 0, 0, 0);
+      const float b0 = r.bias ? __ldg(r.bias + e0) : 0.f, b1 = r.bias ? __ldg(r.bias + e1) : 0.f;
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (q < S) {
+          const uint4 wv0 = w0[q * 32 + lane], wv1 = w1[q * 32 + lane];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint32_t xx = (&xv[q].x)[u >> 1], ww0 = (&wv0.x)[u >> 1], ww1 = (&wv1.x)[u >> 1];
+            const float xf = (u & 1) ? bf16_hi(xx) : bf16_lo(xx);
+            acc0 = __fadd_rn(acc0, __fmul_rn(xf, (u & 1) ? bf16_hi(ww0) : bf16_lo(ww0)));
+            acc1 = __fadd_rn(acc1, __fmul_rn(xf, (u & 1) ? bf16_hi(ww1) : bf16_lo(ww1)));
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        acc0 = __fadd_rn(acc0, __shfl_xor_sync(0xFFFFFFFFu, acc0, off));
+        acc1 = __fadd_rn(acc1, __shfl_xor_sync(0xFFFFFFFFu, acc1, off));
+      }
+      if (r.bias) {
+        acc0 = __fadd_rn(acc0, b0);
+        acc1 = __fadd_rn(acc1, b1);
+      }
+      if (lane < cl_n) {
+        st_cluster_f32(mapa_shared(cl_logit + 4u * uint32_t(t * a.E + e0), uint32_t(lane)), acc0);
+        if (two) st_cluster_f32(mapa_shared(cl_logit + 4u * uint32_t(t * a.E + e1), uint32_t(lane)), acc1);
+      }
     }
   }
 }
@@ -534,12 +591,16 @@ __device__ __forceinline__ void sd_route_logits(const FfnArgs& a, const SdRoute&
 // Top-k of every token by (logit desc, id asc; NaN last), softmax weights, and the stable
 // sort of the pairs by expert, all in shared memory (every CTA computes the same).  All
 // threads; ends with __syncthreads.  CTA 0 writes ids and weights.
+// logits_in_smem: s_logit already holds the logits (the cluster form); else they are read from r.logits.
 __device__ __forceinline__ void sd_route_select(const FfnArgs& a, const SdRoute& r, float* s_logit, int* s_ids,
-                                                float* s_val, float* s_wt, int* s_sp, int* s_off) {
+                                                float* s_val, float* s_wt, int* s_sp, int* s_off,
+                                                bool logits_in_smem = false) {
   const int T = a.T, E = a.E, k = a.k, P = T * k;
   const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < T * E; i += nt) s_logit[i] = __ldcg(r.logits + i);
-  __syncthreads();
+  if (!logits_in_smem) {
+    for (int i = tid; i < T * E; i += nt) s_logit[i] = __ldcg(r.logits + i);
+    __syncthreads();
+  }
   // rank of (t, e) = experts that come before it; the first k ranks are the selection.
   // Four neighbouring threads share a (t, e) and split the comparisons four ways.
   const int n4 = 4 * T * E, n4w = (n4 + 31) & ~31;   // whole warps take part in the shuffles
@@ -549,15 +610,19 @@ __device__ __forceinline__ void sd_route_select(const FfnArgs& a, const SdRoute&
     const int t = i / E, e = i - t * E;
     const float v = s_logit[i];
     const float* row = s_logit + t * E;
-    const int j0 = act ? part * E / 4 : 0, j1 = act ? (part + 1) * E / 4 : 0;
+    // part p compares against j = p, p + 4, ...: the four parts of a warp read four
+    // neighbouring words (no bank conflict), and the counts add up to the same rank
+    const int j1 = act ? E : 0;
     int rank = 0;
     if (!isnan(v)) {
-      for (int j = j0; j < j1; ++j) {
+#pragma unroll 8
+      for (int j = part; j < j1; j += 4) {
         const float u = row[j];
         rank += (u > v) || (u == v && j < e);
       }
     } else {
-      for (int j = j0; j < j1; ++j) rank += !isnan(row[j]) || j < e;
+#pragma unroll 8
+      for (int j = part; j < j1; j += 4) rank += !isnan(row[j]) || j < e;
     }
     rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 1);
     rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 2);
@@ -590,6 +655,7 @@ __device__ __forceinline__ void sd_route_select(const FfnArgs& a, const SdRoute&
   // expert offsets (pairs with a smaller id), then positions (stable within an expert)
   for (int e = tid; e <= E; e += nt) {
     int c = 0;
+#pragma unroll 8
     for (int p = 0; p < P; ++p) c += s_ids[p] < e;
     s_off[e] = c;
   }
@@ -597,6 +663,7 @@ __device__ __forceinline__ void sd_route_select(const FfnArgs& a, const SdRoute&
   for (int p = tid; p < P; p += nt) {
     const int e = s_ids[p];
     int pos = s_off[e];
+#pragma unroll 8
     for (int q = 0; q < p; ++q) pos += s_ids[q] == e;
     s_sp[pos] = p;
   }
@@ -679,7 +746,7 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
     }
     if (warp >= 1 && warp <= kSdCons && ne > 0) {
       if (mbar_wait_warp(bars + 128, 0, s_abort)) {
-        sd_route_logits(a, ra, sm, ne, warp - 1, lane);
+        sd_route_logits(a, ra, sm, ne, warp - 1, lane, b, G);
       } else {
         *s_abort = 1;
       }
@@ -1204,10 +1271,135 @@ __host__ inline bool sl_supported(int E, int d, int f, int fmt, int T, int k, in
   return rows * d * 2 <= (long long)L.stages * L.stage_bytes && f % kSdRowsA == 0;
 }
 
-// NCOL: token columns a lane keeps partial outputs for (1 when T = 1: column 0 only; 2 otherwise)
-template <int FMT, int NCOL>
+// One token (the slice form with NCOL = 1): the top-k of the E logits in s_logit by (logit
+// desc, id asc; NaN last), the weights with the router's arithmetic, then the resident
+// selected experts in ascending id: s_rexp[j] the expert, s_rslot[j] its slot and s_sp[j] its
+// pair (its rank) for j < *s_nres (their tensor scales are the epilogue warp's to load).  This replaces the
+// general selection, pair sort and item scan, whose dependent shared-memory steps dominate a
+// one-token call.  All threads; ends with __syncthreads.
+// logits_in_smem: s_logit already holds the logits (the cluster form); else they are read from r.logits.
+__device__ __forceinline__ void sl_select_t1(const FfnArgs& a, const SdRoute& r, float* s_logit, int* s_ids,
+                                             float* s_val, float* s_wt, const int32_t* s_slot_in, int* s_rexp,
+                                             int* s_rslot, int* s_sp, float* s_ts, uint32_t* s_bits, int* s_nres,
+                                             bool logits_in_smem) {
+  const int E = a.E, k = a.k;
+  const int tid = threadIdx.x, nt = blockDim.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < (E + 31) / 32; i += nt) s_bits[i] = 0u;
+  if (!logits_in_smem) {
+    for (int i = tid; i < E; i += nt) s_logit[i] = __ldcg(r.logits + i);
+    __syncthreads();
+  }
+  // rank of e = experts before it.  E <= 256 with E % 4 == 0: one thread per expert walks the
+  // row with four-wide loads that every lane of a warp shares (a broadcast), four counts in
+  // parallel; otherwise four threads per expert, part p comparing against j = p, p + 4, ...
+  const bool wide = E <= 256 && (E & 3) == 0 && E <= nt;
+  if (wide && tid < E) {
+    const int e = tid;
+    const float v = s_logit[e];
+    const float4* row4 = reinterpret_cast<const float4*>(s_logit);
+    int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+    if (!isnan(v)) {
+#pragma unroll 8
+      for (int j4 = 0; j4 < (E >> 2); ++j4) {
+        const float4 u = row4[j4];
+        const int j = 4 * j4;
+        c0 += (u.x > v) || (u.x == v && j < e);
+        c1 += (u.y > v) || (u.y == v && j + 1 < e);
+        c2 += (u.z > v) || (u.z == v && j + 2 < e);
+        c3 += (u.w > v) || (u.w == v && j + 3 < e);
+      }
+    } else {
+      for (int j = 0; j < E; ++j) c0 += !isnan(s_logit[j]) || j < e;
+    }
+    const int rank = (c0 + c1) + (c2 + c3);
+    if (rank < k) {
+      s_ids[rank] = e;
+      s_val[rank] = v;
+    }
+  }
+  const int n4 = wide ? 0 : 4 * E, n4w = (n4 + 31) & ~31;
+  for (int i4 = tid; i4 < n4w; i4 += nt) {
+    const bool act = i4 < n4;
+    const int e = act ? i4 >> 2 : 0, part = i4 & 3;
+    const float v = s_logit[e];
+    const int j1 = act ? E : 0;
+    int rank = 0;
+    if (!isnan(v)) {
+#pragma unroll 8
+      for (int j = part; j < j1; j += 4) {
+        const float u = s_logit[j];
+        rank += (u > v) || (u == v && j < e);
+      }
+    } else {
+#pragma unroll 8
+      for (int j = part; j < j1; j += 4) rank += !isnan(s_logit[j]) || j < e;
+    }
+    rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 1);
+    rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 2);
+    if (act && part == 0 && rank < k) {
+      s_ids[rank] = e;
+      s_val[rank] = v;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // weights: the router's select-step arithmetic (k <= 32: lane r holds rank r)
+    const float m = s_val[0];
+    float part = 0.f;
+    if (r.renorm) {
+      part = lane < k ? expf(s_val[lane] - m) : 0.f;
+    } else {
+      for (int e = lane; e < E; e += 32) part += expf(s_logit[e] - m);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, off);
+    int e = 0, slot = -1;
+    if (lane < k) {
+      e = s_ids[lane];
+      const float w = expf(s_val[lane] - m) / part;
+      s_wt[lane] = w;
+      if (blockIdx.x == 0) {
+        r.ids[lane] = e;
+        r.tw[lane] = w;
+      }
+      slot = s_slot_in ? s_slot_in[e] : e;
+      if (slot >= a.C) {
+        if (blockIdx.x == 0) set_dev_err(DEV_ERR_BAD_SLOT);
+        slot = -1;
+      }
+      if (slot >= 0) atomicOr(&s_bits[e >> 5], 1u << (e & 31));
+    }
+    __syncwarp();
+    if (slot >= 0) {
+      // position among the resident selected experts in ascending id
+      int pos = __popc(s_bits[e >> 5] & ((1u << (e & 31)) - 1u));
+      for (int w2 = 0; w2 < (e >> 5); ++w2) pos += __popc(s_bits[w2]);
+      s_rexp[pos] = e;
+      s_rslot[pos] = slot;
+      s_sp[pos] = lane;
+    }
+    const int nres = __popc(__ballot_sync(0xFFFFFFFFu, slot >= 0));
+    if (lane == 0) *s_nres = nres;
+  }
+  __syncthreads();
+}
+
+// NCOL: token columns a lane keeps partial outputs for (1 when T = 1: column 0 only; 2 otherwise).
+// CL: the cluster form (launched in clusters of 2 to 8 CTAs, grid a multiple of the cluster):
+//   - the CTAs of a cluster split the router rows (cluster rank r: experts [r E/n, (r+1) E/n)),
+//     write each logit into the shared memory of every CTA of the cluster, and meet at a cluster
+//     barrier: no grid-wide sync before the selection;
+//   - at the end each CTA leaves its partial output in its shared memory; rank r of a cluster
+//     sums slice r of the outputs over the cluster's CTAs in rank order (distributed shared
+//     memory) and writes the cluster's partial of that slice; the last cluster to count in on a
+//     slice (a counter in the workspace header, set back to 0 after use) sums the clusters'
+//     partials in cluster order and writes out.  No CTA waits for another cluster, so the
+//     kernel needs no co-residency beyond its own clusters.
+// Either way the output is the combine's sum regrouped in a fixed order (deterministic).
+template <int FMT, int NCOL, bool CL>
 __global__ void __launch_bounds__(kSdThreads, 1)
-sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, const uint8_t* slices) {
+sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, const uint8_t* slices,
+                unsigned* ccnt) {
   extern __shared__ uint8_t sl_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sl_raw) + 127) & ~uintptr_t(127));
   uint16_t* s_x = reinterpret_cast<uint16_t*>(sm + Ls.off_x);
@@ -1236,6 +1428,7 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
   const uint32_t red_full = bars + 136, red_empty = bars + 152, h_full = bars + 168, h_empty = bars + 184;
   volatile int* s_flag = reinterpret_cast<volatile int*>(sm + Ls.off_bar + 208);
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + Ls.off_bar + 212);
+  volatile int* s_last = reinterpret_cast<volatile int*>(sm + Ls.off_bar + 216);   // cluster form
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = Ls.stages;
   const int G = gridDim.x, b = blockIdx.x;
@@ -1258,40 +1451,78 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
   }
   __syncthreads();
   bool ok = true;
-  const int ne = a.E > b ? (a.E - b + G - 1) / G : 0;   // router rows of this CTA
+  // router rows of this CTA: experts e_first + i * e_step, i < ne
+  const int csz = CL ? int(cluster_nctarank()) : 1, crank = CL ? int(cluster_ctarank()) : 0;
+  const int epc = (a.E + csz - 1) / csz;
+  const int e_first = CL ? crank * epc : b, e_step = CL ? 1 : G;
+  const int ne = CL ? max(0, min(epc, a.E - crank * epc)) : (a.E > b ? (a.E - b + G - 1) / G : 0);
   if (tid == 0 && ne > 0) {
     // router rows are weights: their copy may start before the previous kernel has finished
     mbar_arrive_expect_tx(bars + 128, uint32_t(ne * a.d * 2));
     for (int i = 0; i < ne; ++i)
-      bulk_load(smem_u32(sm + size_t(i) * a.d * 2), ra.wr + size_t(b + i * G) * a.d, uint32_t(a.d * 2), bars + 128);
+      bulk_load(smem_u32(sm + size_t(i) * a.d * 2), ra.wr + size_t(e_first + i * e_step) * a.d, uint32_t(a.d * 2),
+                bars + 128);
   }
+  // every CTA of the cluster has started before any writes into another's shared memory
+  if (CL) asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
   pdl_wait();
   if (a.slot_of)
     for (int e = tid; e < a.E; e += kSdThreads) s_slot[e] = a.slot_of[e];
   if (warp >= 1 && warp <= kSdCons && ne > 0) {
     if (mbar_wait_warp(bars + 128, 0, s_abort)) {
-      sd_route_logits(a, ra, sm, ne, warp - 1, lane);
+      if (CL)
+        sl_route_logits_cl(a, ra, sm, ne, warp - 1, lane, e_first, smem_u32(s_logit), csz);
+      else
+        sd_route_logits(a, ra, sm, ne, warp - 1, lane, e_first, e_step);
     } else {
       *s_abort = 1;
     }
   }
   __syncthreads();
-  if (tid == 0 && !grid_sync_mono(gsync, nullptr)) *s_abort = 1;
-  __syncthreads();
+  if (CL) {
+    cluster_sync_all();   // every logit of the layer is now in this CTA's s_logit
+  } else {
+    if (tid == 0 && !grid_sync_mono(gsync, nullptr)) *s_abort = 1;
+    __syncthreads();
+  }
+  // every CTA of this grid is resident (it passed the barrier above): the next kernel on the
+  // stream may start its prologue on the SMs that this grid frees
+  pdl_launch_dependents();
   if (*s_abort) {
     ok = false;
-    if (tid == 0) set_dev_err(DEV_ERR_GRID_TIMEOUT);
+    if (tid == 0) set_dev_err(CL ? DEV_ERR_TIMEOUT : DEV_ERR_GRID_TIMEOUT);
   }
-  sd_route_select(a, ra, s_logit, s_ids, s_val, s_wt, s_sp, s_off);
-  sd_items(a, s_off, a.slot_of ? s_slot : nullptr, xr, s_a, s_b, s_lo, s_cnt, s_slot, s_scan);   // all threads
-  const int NA = s_a[a.E];
+  const int ua = a.f / kSdRowsA;
+  int* s_nres = s_scan + 40;
+  if (NCOL == 1) {
+    // one token: the resident selected experts in s_a (expert) and s_b (slot), their pairs in s_sp
+    sl_select_t1(a, ra, s_logit, s_ids, s_val, s_wt, a.slot_of ? s_slot : nullptr, s_a, s_b, s_sp, s_ts,
+                 reinterpret_cast<uint32_t*>(s_scan), s_nres, CL);
+  } else {
+    sd_route_select(a, ra, s_logit, s_ids, s_val, s_wt, s_sp, s_off, CL);
+    sd_items(a, s_off, a.slot_of ? s_slot : nullptr, xr, s_a, s_b, s_lo, s_cnt, s_slot, s_scan);   // all threads
+  }
+  const int NA = NCOL == 1 ? *s_nres * ua : s_a[a.E];
+  // item -> (expert, slot, first sorted row, rows, row block): one token by division, else a search
+  auto item_at = [&](SdItem& it, int item) {
+    if (NCOL == 1) {
+      const int j = item / ua;
+      it.e = s_a[j];
+      it.slot = s_b[j];
+      it.lo = j;
+      it.cnt = 1;
+      it.grp = 0;
+      it.n0 = item - j * ua;
+    } else {
+      sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, item, ua);
+    }
+  };
   // items: one token takes b, b + G, ... (every expert shares the staged x); more tokens take a
   // contiguous range (x is restaged per expert)
   const bool strided = a.T == 1;
   const int a_lo = int(unsigned(NA) * unsigned(b) / unsigned(G)), a_hi = int(unsigned(NA) * unsigned(b + 1) / unsigned(G));
   const int first = strided ? b : a_lo, step = strided ? G : 1;
   const int count = strided ? (NA > b ? (NA - b + G - 1) / G : 0) : a_hi - a_lo;
-  const int ua = a.f / kSdRowsA;
   const size_t blk_a = size_t(Ls.blk_a);
   const size_t slot_bytes = sd_slot_bytes(a.d, a.f, FMT);
   const size_t slice_slot = sl_slot_bytes(a.d, a.f);
@@ -1303,7 +1534,7 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
     bool pok = ok;
     SdItem it;
     for (int q = 0; q < count && pok; ++q) {
-      sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, first + q * step, ua);
+      item_at(it, first + q * step);
       if (!mbar_wait_warp(bars + 64 + 8 * stage, ph ^ 1, s_abort)) {
         pok = false;
         break;
@@ -1338,18 +1569,23 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
       }
       if (ne > 0 && !ok) mbar_wait(bars + 128, 0, nullptr);
     }
-    return;
+    goto tail;
   }
 
   if (warp == kSdEpiWarp) {
     // ---------------- epilogue warp: h of each item into s_h ----------------
-    sd_tensor_scales(a, s_a, s_slot, s_ts, lane, 32);
+    if (NCOL != 1) {
+      sd_tensor_scales(a, s_a, s_slot, s_ts, lane, 32);
+    } else if (lane < *s_nres) {   // one token: the resident selected experts s_a[j], slots s_b[j]
+#pragma unroll
+      for (int m3 = 0; m3 < 3; ++m3) s_ts[3 * s_a[lane] + m3] = a.tscale ? a.tscale[s_b[lane] * 3 + m3] : 1.f;
+    }
     __syncwarp();
     bool eok = ok;
     SdItem it;
     int staged_e = -1;
     for (int q = 0; q < count; ++q) {
-      sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, first + q * step, ua);
+      item_at(it, first + q * step);
       if (strided ? q == 0 : it.e != staged_e) {
         sd_work_sync();   // (the consumers stage x and the token group between these)
         sd_work_sync();
@@ -1370,7 +1606,7 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
         const int tok = (lane >> 4) + 2 * j;
         if (eok && tok < n) {
           const float* rb = s_red + buf * Ls.nred;
-#pragma unroll 4
+#pragma unroll 8
           for (int w = 0; w < kSdCons; ++w) {
             gs[j] += rb[((w * 2 + 0) * 16 + (lane & 15)) * xr + tok];
             us[j] += rb[((w * 2 + 1) * 16 + (lane & 15)) * xr + tok];
@@ -1407,10 +1643,11 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
     if (!eok && ok) set_dev_err(DEV_ERR_TIMEOUT);
     sd_work_sync();   // (the consumers write their partial outputs and meet the grid between these)
     sd_work_sync();
-    return;
+    goto tail;
   }
 
   // ---------------- consumers ----------------
+  {
   const int cw = warp - 1;
   const int ct = tid - 32;
   const int g = lane >> 2, t = lane & 3;
@@ -1470,7 +1707,7 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
   const int st_x = a.d + 8;
   SdItem it;
   for (int q = 0; q < count; ++q) {
-    sd_item_first(it, s_a, s_lo, s_cnt, s_slot, a.E, first + q * step, ua);
+    item_at(it, first + q * step);
     const int n = min(xr, it.cnt);
     if (strided ? q == 0 : it.e != staged_e) {
       // the expert's token group: x rows (f16) and tokens (one token: staged once)
@@ -1556,8 +1793,10 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
     }
   }
   if (count > 0) down_part(count - 1, pend_stage, pend_e, pend_w0, pend_w1);
-  // this CTA's partial output [token][row]: this lane holds tokens 2t, 2t + 1 of rows g, g + 8
-  float* pb = ra.part + size_t(b) * a.T * a.d;
+  // this CTA's partial output [token][row]: this lane holds tokens 2t, 2t + 1 of rows g, g + 8.
+  // Grid form: to the workspace; cluster form: to this CTA's shared memory (the ring's bytes:
+  // every staged tile has landed and been read by now).
+  float* pb = CL ? reinterpret_cast<float*>(sm) : ra.part + size_t(b) * a.T * a.d;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     if (i < RP) {
@@ -1573,28 +1812,82 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
     }
   }
   if (!ok) set_dev_err(DEV_ERR_TIMEOUT);
-  sd_work_sync();
-  if (ct == 0) {
-    __threadfence();
-    if (!grid_sync_mono(gsync, s_abort)) {
-      *s_flag = 0;
-      set_dev_err(DEV_ERR_GRID_TIMEOUT);
+  if (CL) {
+    sd_work_sync();   // (the epilogue warp's last two meetings)
+    sd_work_sync();
+  } else {
+    sd_work_sync();
+    if (ct == 0) {
+      __threadfence();
+      if (!grid_sync_mono(gsync, s_abort)) {
+        *s_flag = 0;
+        set_dev_err(DEV_ERR_GRID_TIMEOUT);
+      }
+    }
+    sd_work_sync();
+    if (!*s_flag) return;
+    // outputs [T d b / G, T d (b + 1) / G) of out [T][d]: sum the CTAs' partials in CTA order
+    // (lane-strided, then a fixed butterfly), write out
+    const unsigned nout = unsigned(a.T) * unsigned(a.d);
+    const int o_lo = int(nout * unsigned(b) / unsigned(G)), o_hi = int(nout * unsigned(b + 1) / unsigned(G));
+    for (int o = o_lo + cw; o < o_hi; o += kSdCons) {
+      // this lane's partials c = lane, lane + 32, ... loaded together, then added in that order
+      float v = 0.f;
+      for (int c0 = lane; c0 < G; c0 += 32 * 8) {
+        float pv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pv[u] = c0 + 32 * u < G ? __ldcg(ra.part + size_t(c0 + 32 * u) * nout + o) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (c0 + 32 * u < G) v += pv[u];
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+      if (lane == 0) {
+        ra.out_f32[o] = v;
+        if (ra.out_bf16) ra.out_bf16[o] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      }
     }
   }
-  sd_work_sync();
-  if (!*s_flag) return;
-  // outputs [T d b / G, T d (b + 1) / G) of out [T][d]: sum the CTAs' partials in CTA order
-  // (lane-strided, then a fixed butterfly), write out
-  const unsigned nout = unsigned(a.T) * unsigned(a.d);
-  const int o_lo = int(nout * unsigned(b) / unsigned(G)), o_hi = int(nout * unsigned(b + 1) / unsigned(G));
-  for (int o = o_lo + cw; o < o_hi; o += kSdCons) {
-    float v = 0.f;
-    for (int c = lane; c < G; c += 32) v += __ldcg(ra.part + size_t(c) * nout + o);
+  }   // consumers
+tail:
+  if (CL) {
+    cluster_sync_all();   // every CTA of the cluster has its partial in shared memory
+    const int n = a.T * a.d, ncl = G / csz, cid = b / csz;
+    const int lo = int((long long)n * crank / csz), hi = int((long long)n * (crank + 1) / csz);
+    const uint32_t part0 = smem_u32(sm);
+    float* cpart = ra.part + size_t(cid) * n;
+    for (int o = lo + tid; o < hi; o += kSdThreads) {
+      float pv[8];   // the cluster's partials of output o, loaded together, added in rank order
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-    if (lane == 0) {
-      ra.out_f32[o] = v;
-      if (ra.out_bf16) ra.out_bf16[o] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      for (int q = 0; q < 8; ++q) pv[q] = q < csz ? ld_cluster_f32(mapa_shared(part0 + 4u * uint32_t(o), uint32_t(q))) : 0.f;
+      float v = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < csz) v += pv[q];
+      cpart[o] = v;
+    }
+    __syncthreads();
+    if (tid == 0)   // (release: the barrier above orders the CTA's cluster-partial writes before it)
+      *s_last = atom_add_acq_rel(ccnt + crank, 1u) == unsigned(ncl - 1);
+    __syncthreads();
+    cluster_sync_all();   // no CTA leaves while another still reads its shared memory
+    if (*s_last) {
+      // slice [lo, hi) of out: the clusters' partials in cluster order
+      for (int o = lo + tid; o < hi; o += kSdThreads) {
+        float v = 0.f;   // in cluster order, sixteen loads in flight at a time
+        for (int c0 = 0; c0 < ncl; c0 += 16) {
+          float pv[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) pv[u] = c0 + u < ncl ? __ldcg(ra.part + size_t(c0 + u) * n + o) : 0.f;
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            if (c0 + u < ncl) v += pv[u];
+        }
+        ra.out_f32[o] = v;
+        if (ra.out_bf16) ra.out_bf16[o] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      }
+      if (tid == 0) ccnt[crank] = 0u;   // zero again for the next call on this workspace
     }
   }
 }

@@ -1,7 +1,9 @@
 // ftmoe C ABI: argument checks, workspace layout and kernel launches.
 // All kernels live in this one translation unit (they share the device error word).
+#include <array>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <new>
 
@@ -630,7 +632,9 @@ bool lru_alloc(int L, int E, int C, LruState* st, void** mem) {
 // `fmt`), for slot copies.  The prepared layouts are copied part by part (their part
 // offsets depend on each arena's slot count).  Returns the count, or -1 if the prepared
 // buffers are not both present or both absent.
-int slot_regions(const ftmoe_layer_desc* d, const ftmoe_weights* src, const ftmoe_weights* dst, SlotRegion* r) {
+// parts: bit 0 = the prefill part of the prepared layout, bit 1 = the decode parts.
+int slot_regions(const ftmoe_layer_desc* d, const ftmoe_weights* src, const ftmoe_weights* dst, SlotRegion* r,
+                 int parts = 3) {
   int n = 0;
   auto add = [&](const void* s, void* t, size_t ss, size_t ts, size_t bytes) {
     if (!bytes) return;
@@ -666,12 +670,12 @@ int slot_regions(const ftmoe_layer_desc* d, const ftmoe_weights* src, const ftmo
   const uint8_t* sp = static_cast<const uint8_t*>(src->prepared);
   uint8_t* tp = static_cast<uint8_t*>(const_cast<void*>(dst->prepared));
   const int sC = src->C, tC = dst->C;
-  if (prep_prefill_bytes(d, 1)) {
+  if ((parts & 1) && prep_prefill_bytes(d, 1)) {
     const size_t gu = prep_gate_up_bytes(d, 1), dn = prep_down_bytes(d, 1);
     add(sp, tp, gu, gu, gu);
     add(sp + align1k(prep_gate_up_bytes(d, sC)), tp + align1k(prep_gate_up_bytes(d, tC)), dn, dn, dn);
   }
-  if (prep_decode_bytes(d, 1)) {
+  if ((parts & 2) && prep_decode_bytes(d, 1)) {
     const size_t db = sd_slot_bytes(d->d, d->ffn, d->fmt);
     add(sp + prep_decode_offset(d, sC), tp + prep_decode_offset(d, tC), db, db, db);
     if (prep_slices_bytes(d, 1)) {
@@ -1015,14 +1019,88 @@ bool layer_slice_ok(const ftmoe_layer_desc* d, const ftmoe_weights* w, int T) {
   if (T > 1 && d->fmt != FTMOE_NVFP4) return false;
   return sl_supported(d->E, d->d, d->ffn, d->fmt, T, d->k, num_sms(), max_smem_optin());
 }
+// Cluster form of the slice kernel: among cluster sizes 8, 4 and 2 whose CTAs each hold their
+// share of the router rows in the ring, the one that places the most CTAs on the GPU (as many
+// clusters as fit, one CTA per SM; on a tie the larger cluster).  More CTAs means fewer items
+// per CTA, and an item beyond the ring's stages would wait for a stage to free.  {0, 0}: the
+// grid form.  Cached per shape.
+struct SlClusterPlan {
+  int cs, grid;
+};
+template <int FMT, int NCOL>
+SlClusterPlan sl_cluster_plan(const FfnArgs& a, const SlLayout& Ls) {
+  static std::mutex mu;
+  static std::map<std::array<int, 5>, SlClusterPlan> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const std::array<int, 5> key{dev, a.E, a.d, a.T, Ls.smem};
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  SlClusterPlan plan{0, 0};
+  auto kern = sl_layer_kernel<FMT, NCOL, true>;
+  if (resident_ctas(kern, kSdThreads, size_t(Ls.smem)) >= 1) {
+    for (int cs : {8, 4, 2}) {
+      const long long epc = (a.E + cs - 1) / cs;
+      if (epc * a.d * 2 > (long long)Ls.stages * Ls.stage_bytes || num_sms() < cs) continue;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(num_sms() / cs * cs);
+      cfg.blockDim = dim3(kSdThreads);
+      cfg.dynamicSmemBytes = size_t(Ls.smem);
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = unsigned(cs);
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        continue;
+      }
+      const int grid = std::min(n, num_sms() / cs) * cs;
+      if (n >= 1 && grid > plan.grid) plan = SlClusterPlan{cs, grid};
+    }
+  }
+  cache[key] = plan;
+  return plan;
+}
+
 template <int FMT, int NCOL>
 ftmoe_status layer_slice_launch(const FfnArgs& a, const SdRoute& r, void* hdr, const uint8_t* slices,
                                 cudaStream_t st) {
   const SlLayout Ls = sl_layout(a.E, a.d, FMT, a.T, a.k, max_smem_optin());
-  if (resident_ctas(sl_layer_kernel<FMT, NCOL>, kSdThreads, size_t(Ls.smem)) < 1) return FTMOE_ERR_CUDA;
   unsigned long long* gs = reinterpret_cast<unsigned long long*>(static_cast<char*>(hdr) + kWsGridSync);
-  return launch(sl_layer_kernel<FMT, NCOL>, dim3(num_sms()), dim3(kSdThreads), size_t(Ls.smem), st, a, Ls, r, gs,
-                slices);
+  unsigned* ccnt = reinterpret_cast<unsigned*>(static_cast<char*>(hdr) + kWsClusterCnt);
+  const SlClusterPlan plan = sl_cluster_plan<FMT, NCOL>(a, Ls);
+  if (plan.cs > 0) {
+    // the function's dynamic shared-memory bound is per function, and launches of other
+    // shapes may have lowered it since the plan was made
+    if (cudaFuncSetAttribute(sl_layer_kernel<FMT, NCOL, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Ls.smem) != cudaSuccess)
+      return FTMOE_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.grid);
+    cfg.blockDim = dim3(kSdThreads);
+    cfg.dynamicSmemBytes = size_t(Ls.smem);
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = unsigned(plan.cs);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, sl_layer_kernel<FMT, NCOL, true>, a, Ls, r, gs, slices, ccnt) == cudaSuccess
+               ? FTMOE_OK
+               : FTMOE_ERR_CUDA;
+  }
+  if (resident_ctas(sl_layer_kernel<FMT, NCOL, false>, kSdThreads, size_t(Ls.smem)) < 1) return FTMOE_ERR_CUDA;
+  return launch(sl_layer_kernel<FMT, NCOL, false>, dim3(num_sms()), dim3(kSdThreads), size_t(Ls.smem), st, a, Ls, r,
+                gs, slices, ccnt);
 }
 template <int FMT>
 ftmoe_status layer_fused_launch(const FfnArgs& a, const SdRoute& r, void* hdr, cudaStream_t st) {
@@ -1164,6 +1242,105 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
 }  // extern "C"
 
 // =============================================================================
+// ftmoe_layer_forward_host: staging of x and of the bf16 output in the workspace, after the
+// layer call's own bytes.
+// =============================================================================
+extern "C" size_t ftmoe_layer_host_workspace_size(const ftmoe_layer_desc* d, int T) {
+  if (!desc_ok(d) || T < 1 || T > kMaxT) return 0;
+  return align256(layer_ws(d, T).total) + 2 * align256(size_t(T) * d->d * 2);
+}
+
+extern "C" ftmoe_status ftmoe_layer_forward_host(const ftmoe_layer_desc* d, const ftmoe_weights* w,
+                                                 const int32_t* slot_of, const uint16_t* x_host, const uint16_t* wr,
+                                                 const float* bias, int T, int32_t* ids, float* tw, float* out_f32,
+                                                 uint16_t* out_host, void* ws, size_t ws_bytes, void* stream) {
+  if (!desc_ok(d) || T < 1 || T > kMaxT || !x_host || !out_host || !ws) return FTMOE_ERR_INVALID_ARG;
+  const size_t need = ftmoe_layer_host_workspace_size(d, T);
+  if (ws_bytes < need) return FTMOE_ERR_WORKSPACE;
+  const size_t base = align256(layer_ws(d, T).total), xb = size_t(T) * d->d * 2;
+  char* p = static_cast<char*>(ws);
+  uint16_t* x_dev = reinterpret_cast<uint16_t*>(p + base);
+  uint16_t* o_dev = reinterpret_cast<uint16_t*>(p + base + align256(xb));
+  cudaStream_t st = as_stream(stream);
+  if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess) return FTMOE_ERR_CUDA;
+  const ftmoe_status s =
+      ftmoe_layer_forward(d, w, slot_of, x_dev, wr, bias, T, ids, tw, out_f32, o_dev, ws, base, stream);
+  if (s != FTMOE_OK) return s;
+  return cudaMemcpyAsync(out_host, o_dev, xb, cudaMemcpyDeviceToHost, st) == cudaSuccess ? FTMOE_OK : FTMOE_ERR_CUDA;
+}
+
+// =============================================================================
+// ftmoe_layers_streamed: L layers whose experts stream from a host pool through one or two
+// device arenas; with two, layer l+1's experts are copied while layer l computes.
+// =============================================================================
+extern "C" ftmoe_status ftmoe_layers_streamed(const ftmoe_layer_desc* d, int L, const ftmoe_weights* pool,
+                                              const ftmoe_weights* arenas, int n_arenas, const uint16_t* const* x,
+                                              const uint16_t* const* wr, const float* const* bias, int T,
+                                              float* const* out_f32, uint16_t* const* out_bf16, void* ws,
+                                              size_t ws_bytes, void* compute_stream, void* copy_stream) {
+  if (!desc_ok(d) || L < 1 || T < 1 || T > kMaxT || !pool || !arenas || n_arenas < 1 || n_arenas > 2)
+    return FTMOE_ERR_INVALID_ARG;
+  if (!x || !wr || !out_f32 || !ws || !x[0]) return FTMOE_ERR_INVALID_ARG;
+  if (!weights_ok(d, pool) || (long long)pool->C < (long long)L * d->E) return FTMOE_ERR_INVALID_ARG;
+  for (int b = 0; b < n_arenas; ++b)
+    if (!weights_ok(d, &arenas[b]) || arenas[b].C < d->E) return FTMOE_ERR_INVALID_ARG;
+  for (int l = 0; l < L; ++l) {
+    if (!wr[l] || !out_f32[l]) return FTMOE_ERR_INVALID_ARG;
+    if (!x[l] && (l == 0 || !out_bf16 || !out_bf16[l - 1])) return FTMOE_ERR_INVALID_ARG;
+  }
+  if (ws_bytes < layer_ws(d, T).total) return FTMOE_ERR_WORKSPACE;
+  // what the call's path reads: the canonical arrays, plus the prefill part (tensor-core NVFP4
+  // path) or the decode parts (decode path) of the prepared layout
+  const int parts = ffn_path(d, T) == 1 ? 1 : (ffn_path(d, T) == 0 ? 2 : 0);
+  SlotRegion reg[kMaxSlotRegions];
+  const int nr = slot_regions(d, pool, &arenas[0], reg, parts);
+  if (nr < 0) return FTMOE_ERR_INVALID_ARG;
+  for (int b = 1; b < n_arenas; ++b) {
+    SlotRegion other[kMaxSlotRegions];
+    if (slot_regions(d, pool, &arenas[b], other, parts) != nr) return FTMOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t cs = as_stream(compute_stream), ps = as_stream(copy_stream);
+  cudaEvent_t filled[2] = {nullptr, nullptr}, done[2] = {nullptr, nullptr};
+  ftmoe_status s = FTMOE_OK;
+  for (int b = 0; b < n_arenas && s == FTMOE_OK; ++b)
+    if (cudaEventCreateWithFlags(&filled[b], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&done[b], cudaEventDisableTiming) != cudaSuccess)
+      s = FTMOE_ERR_CUDA;
+  // the copy stream starts after whatever the compute stream has queued (the arenas may be in use)
+  if (s == FTMOE_OK && (cudaEventRecord(done[0], cs) != cudaSuccess || cudaStreamWaitEvent(ps, done[0], 0) != cudaSuccess))
+    s = FTMOE_ERR_CUDA;
+  const size_t E = size_t(d->E);
+  for (int l = 0; l < L && s == FTMOE_OK; ++l) {
+    const int b = l % n_arenas;
+    const ftmoe_weights* A = &arenas[b];
+    SlotRegion rb[kMaxSlotRegions];
+    slot_regions(d, pool, A, rb, parts);
+    if (l >= n_arenas && cudaStreamWaitEvent(ps, done[b], 0) != cudaSuccess) {
+      s = FTMOE_ERR_CUDA;
+      break;
+    }
+    // layer l's experts are slots l*E .. l*E + E - 1 of the pool: one contiguous range per array
+    for (int i = 0; i < nr && s == FTMOE_OK; ++i)
+      if (cudaMemcpyAsync(rb[i].dst, rb[i].src + size_t(l) * E * rb[i].src_stride, E * rb[i].bytes,
+                          cudaMemcpyDefault, ps) != cudaSuccess)
+        s = FTMOE_ERR_CUDA;
+    if (s != FTMOE_OK || cudaEventRecord(filled[b], ps) != cudaSuccess || cudaStreamWaitEvent(cs, filled[b], 0) != cudaSuccess) {
+      s = FTMOE_ERR_CUDA;
+      break;
+    }
+    const uint16_t* xl = x[l] ? x[l] : out_bf16[l - 1];
+    s = ftmoe_layer_forward(d, A, nullptr, xl, wr[l], bias ? bias[l] : nullptr, T, nullptr, nullptr, out_f32[l],
+                            out_bf16 ? out_bf16[l] : nullptr, ws, ws_bytes, compute_stream);
+    if (s == FTMOE_OK && cudaEventRecord(done[b], cs) != cudaSuccess) s = FTMOE_ERR_CUDA;
+  }
+  for (int b = 0; b < 2; ++b) {   // destroyed once their pending work completes
+    if (filled[b]) cudaEventDestroy(filled[b]);
+    if (done[b]) cudaEventDestroy(done[b]);
+  }
+  return s;
+}
+
+// =============================================================================
 // ftmoe_route_noalloc: the router for callers that cannot allocate device memory.
 //
 // Its scratch (the completion counter and the [T][E] fp32 logits) lives in one
@@ -1180,17 +1357,47 @@ static __device__ __align__(256) unsigned char g_route_noalloc_scratch[FTMOE_WS_
 namespace {
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices];
+unsigned long long g_noalloc_ctx[kMaxDevices];   // the context the address was taken in
 
-// Device address of the fixed scratch array on the current device (set up once per device).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the current context (0 if the driver cannot tell).  A device reset ends the
+// context and reloads this library's module in the next one, at a possibly different address.
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_cur || !get_id || get_cur(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the fixed scratch array on the current device: looked up on the first call
+// in each context of a device (after a device reset, again), then reused.  While no context is
+// current yet (id 0) it is looked up on every call; the lookup makes the context current.
 ftmoe_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FTMOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FTMOE_ERR_UNSUPPORTED;
+  const unsigned long long ctx = current_ctx_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_noalloc_ptr[dev] || ctx == 0 || g_noalloc_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_route_noalloc_scratch) != cudaSuccess || !p) return FTMOE_ERR_CUDA;
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = ctx;
   }
   *out = g_noalloc_ptr[dev];
   return FTMOE_OK;

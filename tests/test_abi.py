@@ -367,3 +367,36 @@ def test_miss_split_and_resize_check_their_arguments_on_the_host(L):
     assert L.ftmoe_miss_split(None, 0, 16, 1, 8, 16, 1.0, 2.0, -1, 16, 16, 16, 16, 16, None) == 1
     assert L.ftmoe_lru_resize(None, 4, None, None, None) == 1
     assert L.ftmoe_lru_capacity(None) == -1
+
+
+def test_host_buffer_layer_call_checks(L):
+    d = ft.desc(128, 8, 2048, 768, ft.NVFP4)
+    need = L.ftmoe_layer_host_workspace_size(ctypes.byref(d), 4)
+    assert need >= L.ftmoe_layer_workspace_size(ctypes.byref(d), 4) + 2 * 4 * 2048 * 2
+    w = _ws(8, d=2048, f=768)
+    args = [ctypes.byref(d), ctypes.byref(w), None, 16, 16, None, 4, 16, 16, 16, 16, 16]
+    assert L.ftmoe_layer_forward_host(*args, need - 1, None) == 4             # workspace too small
+    bad = list(args)
+    bad[3] = None                                                             # no host input
+    assert L.ftmoe_layer_forward_host(*bad, need, None) == 1
+    bad = list(args)
+    bad[10] = None                                                            # no host output
+    assert L.ftmoe_layer_forward_host(*bad, need, None) == 1
+
+
+def test_streamed_layers_check_their_arguments_on_the_host(L):
+    d = ft.desc(16, 4, 256, 256, ft.NVFP4)
+    pool, arena = _ws(48), _ws(16)
+    arenas = (ft.WeightsStruct * 2)(arena, arena)
+    P3 = ctypes.c_void_p * 3
+    xs, wr, of = P3(16, 16, 16), P3(16, 16, 16), P3(16, 16, 16)
+    ws = L.ftmoe_layer_workspace_size(ctypes.byref(d), 300)
+    call = lambda **kw: L.ftmoe_layers_streamed(
+        ctypes.byref(d), kw.get("L", 3), ctypes.byref(kw.get("pool", pool)), arenas, kw.get("n", 2), kw.get("xs", xs),
+        wr, None, 300, of, None, 16, kw.get("ws", ws), None, None)
+    assert call(n=3) == 1                                   # one or two arenas
+    assert call(n=0) == 1
+    assert call(pool=_ws(47)) == 1                          # the pool holds fewer than L*E slots
+    assert call(xs=P3(16, None, 16)) == 1                   # a chained layer without bf16 outputs
+    assert call(xs=P3(None, 16, 16)) == 1                   # the first layer needs an input
+    assert call(ws=ws - 1) == 4

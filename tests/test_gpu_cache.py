@@ -147,7 +147,7 @@ def _check_slots(pool, arena, pairs, prepared=True, dsc=None):
     preparation of an arena holding the same slots (unfilled slots zero on both sides)."""
     for name in NAMES:
         P, A = getattr(pool, name), getattr(arena, name)
-        if P is None:
+        if P is None or (name == "glob" and pool.fmt != synth.NVFP4):   # tensor scales: NVFP4 only
             continue
         for s, t in pairs:
             assert torch.equal(A[t].cpu(), P[s].cpu()), (name, s, t)

@@ -72,6 +72,7 @@ CASES = [
     (synth.MXFP4, 32, 6, 512, 256, 1, 1, 1.0),
     (synth.MXFP4, 32, 6, 256, 512, 5, 0, 0.0),
     (synth.NVFP4, 300, 2, 256, 128, 2, 0, 0.0),   # more experts than SMs: two router rows per CTA
+    (synth.NVFP4, 1024, 4, 256, 128, 1, 1, 1.1),  # router rows too many for a cluster's share: the grid form
 ]
 
 
@@ -224,4 +225,32 @@ def test_slice_form_skipped_experts_and_repeated_calls(fmt):
                 assert rel_l2(of.cpu().numpy(), ref["out"]) < TOL
                 _, _, of_s, _ = _separate(dsc, W, slot, x, wr, None)
                 assert _same(2, of, of_s)
+    assert ft.get_device_error() == 0
+
+
+@pytest.mark.parametrize("fmt,T", [(synth.NVFP4, 1), (synth.MXFP4, 3)])
+def test_host_buffer_call_equals_the_device_call(fmt, T):
+    """ftmoe_layer_forward_host (x from pinned host memory, bf16 output back to it) gives the
+    device call's outputs bit for bit, twice in a row on one workspace."""
+    E, k, d, f = 32, 4, 512, 256
+    W = synth.make_experts(fmt, E, d, f, 77, device="cuda")
+    dsc = ft.desc(E, k, d, f, fmt)
+    ft.prepare_weights(dsc, W)
+    wr = synth.make_router(E, d, 77, device="cuda")
+    st = ft.weights_struct(W)
+    ws = ft.workspace(ft.layer_host_workspace_size(dsc, T))
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    of = torch.empty(T, d, dtype=torch.float32, device="cuda")
+    for seed in (5, 6):
+        x = synth.make_x(T, d, seed)
+        xh = x.pin_memory()
+        oh = torch.full((T, d), float("nan"), dtype=torch.bfloat16).pin_memory()
+        call = ft.LayerHostCall(dsc, st, None, xh, wr, None, ids, w, of, oh, ws)
+        call()
+        torch.cuda.synchronize()
+        ids_d, w_d, of_d, ob_d = _layer(dsc, W, None, x.cuda(), wr, None)
+        assert torch.equal(ids, ids_d) and torch.equal(w, w_d)
+        assert torch.equal(of, of_d)
+        assert torch.equal(oh, ob_d.cpu())
     assert ft.get_device_error() == 0

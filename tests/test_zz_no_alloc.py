@@ -60,3 +60,24 @@ def test_route_noalloc_rejects_sizes_beyond_its_array():
     T = 257                                   # 257 * 1024 logits > the 262144-entry array
     st = ft.lib().ftmoe_route_noalloc(ctypes.byref(dsc), 16, 16, None, T, 16, 16, None)
     assert st == 4                            # FTMOE_ERR_WORKSPACE, before any device work
+
+
+def test_route_noalloc_fills_its_array_exactly_and_matches_the_oracle():
+    """T * E equal to the array's capacity (256 tokens x 1024 experts, top-32: the path where a
+    second kernel selects), twice in a row: ids bit for bit and weights against ftmoe_route and
+    against the oracle's router (oracle/route.py)."""
+    from oracle.route import route as oracle_route
+    from helpers import bf16_bits
+    E, k, d, T = 1024, 32, 256, 256
+    assert T * E == 262144                    # FTMOE_NOALLOC_MAX_LOGITS
+    dsc = ft.desc(E, k, d, 128, synth.BF16, 1)
+    for seed in (7, 8):
+        x = synth.make_x(T, d, seed).cuda()
+        wr = synth.make_router(E, d, seed).cuda()
+        ids, w = _noalloc(dsc, x, wr, None)
+        r_ids, r_w, _ = route(dsc, x, wr, None)
+        assert np.array_equal(ids.cpu().numpy(), r_ids.cpu().numpy())
+        np.testing.assert_allclose(w.cpu().numpy(), r_w.cpu().numpy(), rtol=2e-6, atol=1e-7)
+        o_ids, o_w, _ = oracle_route(bf16_bits(x.cpu()), bf16_bits(wr.cpu()), None, k, 1)
+        assert np.array_equal(ids.cpu().numpy(), o_ids)
+        np.testing.assert_allclose(w.cpu().numpy(), o_w, rtol=2e-6, atol=1e-7)
