@@ -520,6 +520,13 @@ const char* ftmoe_status_string(ftmoe_status s);
 /* Reads and clears the device error word (synchronises `stream`).
  * *code = 0 if no device-side check failed since the last read. */
 ftmoe_status ftmoe_get_device_error(int* code, void* stream);
+/* Sets the time after which every bounded device wait of the library gives up (grid and
+ * cluster-partial counters, shared-memory barriers, readiness counts): ns, or 0 for the default
+ * 2 s.  A wait that gives up sets the device error word (codes 6 and 10 are timeouts) and the
+ * kernel winds down without trapping; after one, zero the workspace's first
+ * FTMOE_WS_ZERO_BYTES bytes before its next use.  Synchronous; applies to later launches on
+ * the current device.  For tests and diagnostics that make a wait run out. */
+ftmoe_status ftmoe_set_wait_limit(unsigned long long ns);
 /* Library version, e.g. 100 = 0.1.0. */
 int ftmoe_version(void);
 

@@ -35,7 +35,7 @@ EXPORTS = [
     "ftmoe_layer_workspace_size", "ftmoe_layer_path", "ftmoe_layer_forward", "ftmoe_status_string", "ftmoe_get_device_error",
     "ftmoe_version", "ftmoe_copy_slots", "ftmoe_qstar", "ftmoe_qstar_fill_count", "ftmoe_miss_split",
     "ftmoe_lru_capacity", "ftmoe_lru_resize", "ftmoe_layer_host_workspace_size", "ftmoe_layer_forward_host",
-    "ftmoe_layers_streamed",
+    "ftmoe_layers_streamed", "ftmoe_set_wait_limit",
 ]
 
 
@@ -105,6 +105,7 @@ def lib() -> ctypes.CDLL:
         "ftmoe_layer_host_workspace_size": (_SZ, [_P, _I]),
         "ftmoe_layer_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
         "ftmoe_layers_streamed": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P, _P]),
+        "ftmoe_set_wait_limit": (_I, [ctypes.c_ulonglong]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -362,6 +363,11 @@ def layer_forward(dsc, wstruct, slot_of, x, w_router, bias, ids, topk_w, out_f32
     _check(lib().ftmoe_layer_forward(ctypes.byref(dsc), ctypes.byref(wstruct), _ptr(slot_of), _ptr(x),
                                      _ptr(w_router), _ptr(bias), T, _ptr(ids), _ptr(topk_w), _ptr(out_f32),
                                      _ptr(out_bf16), _ptr(ws), _ws_bytes(ws), _stream(stream)), "ftmoe_layer_forward")
+
+
+def set_wait_limit(ns: int = 0):
+    """ftmoe_set_wait_limit: the time (ns) after which a bounded device wait gives up; 0 = 2 s."""
+    _check(lib().ftmoe_set_wait_limit(int(ns)), "ftmoe_set_wait_limit")
 
 
 def get_device_error(stream=None) -> int:

@@ -469,11 +469,11 @@ __device__ __forceinline__ bool grid_sync_mono(unsigned long long* w, volatile i
   const unsigned long long G = gridDim.x;
   const unsigned long long old = atom_add_release_u64(w, 1ull);
   const unsigned long long target = (old / G + 1) * G;
-  const unsigned long long t0 = globaltimer_ns();
+  const unsigned long long t0 = globaltimer_ns(), lim = wait_limit_ns();
   for (uint32_t it = 0; ld_acquire_u64(w) < target; ++it) {
     if ((it & 63u) == 63u) {
       if (abort && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (globaltimer_ns() - t0 > lim) return false;
     }
   }
   return true;
@@ -481,11 +481,11 @@ __device__ __forceinline__ bool grid_sync_mono(unsigned long long* w, volatile i
 
 // Waits until *v >= target (bounded); false = gave up.
 __device__ __forceinline__ bool wait_count(const unsigned* v, unsigned target, volatile int* abort) {
-  const unsigned long long t0 = globaltimer_ns();
+  const unsigned long long t0 = globaltimer_ns(), lim = wait_limit_ns();
   for (uint32_t it = 0; ld_acquire_u32(v) < target; ++it) {
     if ((it & 63u) == 63u) {
       if (abort && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (globaltimer_ns() - t0 > lim) return false;
     }
   }
   return true;
@@ -1289,30 +1289,33 @@ __device__ __forceinline__ void sl_select_t1(const FfnArgs& a, const SdRoute& r,
     for (int i = tid; i < E; i += nt) s_logit[i] = __ldcg(r.logits + i);
     __syncthreads();
   }
-  // rank of e = experts before it.  E <= 256 with E % 4 == 0: one thread per expert walks the
-  // row with four-wide loads that every lane of a warp shares (a broadcast), four counts in
-  // parallel; otherwise four threads per expert, part p comparing against j = p, p + 4, ...
-  const bool wide = E <= 256 && (E & 3) == 0 && E <= nt;
-  if (wide && tid < E) {
-    const int e = tid;
+  // rank of e = experts before it, four threads per expert.  When E % 16 == 0 and 4 E threads
+  // fit the block, thread (e, q) reads four-wide words 4i + q of the row: the four q of a warp
+  // hit four different bank groups and the eight experts of a warp share each load (a
+  // broadcast).  Otherwise part p compares against j = p, p + 4, ...
+  const bool wide = (E & 15) == 0 && 4 * E <= nt;
+  if (wide && tid < 4 * E) {
+    const int e = tid >> 2, q = tid & 3;
     const float v = s_logit[e];
     const float4* row4 = reinterpret_cast<const float4*>(s_logit);
     int c0 = 0, c1 = 0, c2 = 0, c3 = 0;
     if (!isnan(v)) {
 #pragma unroll 8
-      for (int j4 = 0; j4 < (E >> 2); ++j4) {
+      for (int i = 0; i < (E >> 4); ++i) {
+        const int j4 = 4 * i + q, j = 4 * j4;
         const float4 u = row4[j4];
-        const int j = 4 * j4;
         c0 += (u.x > v) || (u.x == v && j < e);
         c1 += (u.y > v) || (u.y == v && j + 1 < e);
         c2 += (u.z > v) || (u.z == v && j + 2 < e);
         c3 += (u.w > v) || (u.w == v && j + 3 < e);
       }
     } else {
-      for (int j = 0; j < E; ++j) c0 += !isnan(s_logit[j]) || j < e;
+      for (int j = q; j < E; j += 4) c0 += !isnan(s_logit[j]) || j < e;
     }
-    const int rank = (c0 + c1) + (c2 + c3);
-    if (rank < k) {
+    int rank = (c0 + c1) + (c2 + c3);
+    rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 1);
+    rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 2);
+    if (q == 0 && rank < k) {
       s_ids[rank] = e;
       s_val[rank] = v;
     }

@@ -706,6 +706,11 @@ const char* ftmoe_status_string(ftmoe_status s) {
   return "unknown status";
 }
 
+ftmoe_status ftmoe_set_wait_limit(unsigned long long ns) {
+  const unsigned long long v = ns ? ns : kWaitLimitNs;
+  return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v)) == cudaSuccess ? FTMOE_OK : FTMOE_ERR_CUDA;
+}
+
 ftmoe_status ftmoe_get_device_error(int* code, void* stream) {
   if (!code) return FTMOE_ERR_INVALID_ARG;
   cudaStream_t st = as_stream(stream);

@@ -2,7 +2,8 @@
 // tile loads, tensor memory (TMEM) allocation, tcgen05 MMA issue, scale-factor
 // copies and accumulator loads.
 //
-// Every wait is bounded.  A wait that runs past kWaitLimitNs returns false;
+// Every wait is bounded.  A wait that runs past the wait limit (wait_limit_ns, 2 s unless
+// ftmoe_set_wait_limit changed it) returns false;
 // the caller records FTMOE_ERR_TIMEOUT in the device error word and winds
 // down instead of spinning forever.
 #pragma once
@@ -11,7 +12,12 @@
 
 namespace ftmoe {
 
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s, the default
+// The limit every bounded wait applies (set by ftmoe_set_wait_limit; read when a wait begins).
+__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+__device__ __forceinline__ unsigned long long wait_limit_ns() {
+  return *reinterpret_cast<volatile unsigned long long*>(&g_wait_limit_ns);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -86,12 +92,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // (time limit, or *abort became non-zero while waiting).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
+  const unsigned long long t0 = globaltimer_ns(), lim = wait_limit_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (abort && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (globaltimer_ns() - t0 > lim) return false;
     }
   }
 }
