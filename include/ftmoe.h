@@ -168,6 +168,15 @@ ftmoe_status ftmoe_prepare_weights(const ftmoe_layer_desc* desc, const ftmoe_wei
  *     Each product is exact; each add is rounded to fp32.
  *   - The 32 lane sums combine by an xor butterfly over offsets 16, 8, 4, 2, 1.
  *   - The bias is added last.
+ * Long batches (logits NULL, T >= 256, desc->renorm, E a multiple of 16 in
+ * 16..256, d <= 4096) run the logits on tcgen05 tensor cores.  A per-token
+ * error bound (relative 2 * (d/16 * 2^-22 + (d/32 + 5) * 2^-24) of
+ * ||x|| max_e ||w_e||) keeps as candidates the experts within the bound of the
+ * k-th value; their logits are recomputed in order R and the top-k taken from
+ * them, so ids and weights equal those above bit for bit.  Tokens with more
+ * than 32 candidates are recomputed entirely in order R.  The workspace's
+ * uint32 at byte 96 then counts those tokens, and the uint32 at byte 100 the
+ * tokens with more than k candidates.
  * Preconditions: 1 <= T <= 2^20, d % 256 == 0.
  * ------------------------------------------------------------------------- */
 size_t ftmoe_route_workspace_size(const ftmoe_layer_desc* desc, int T);

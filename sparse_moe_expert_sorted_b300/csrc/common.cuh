@@ -50,6 +50,10 @@ constexpr size_t kWsGridSync = 24;
 // uint32 [8]: per output slice, the clusters that have added their partial (the cluster form
 // of the one-kernel decode layer; the last one sums and sets it back to 0).
 constexpr size_t kWsClusterCnt = 64;
+// uint32: tokens the tensor-core router left to its full order-R fallback, and tokens for which
+// it recomputed more than k logits in order R (both set by each such call).
+constexpr size_t kWsRouteFallback = 96;
+constexpr size_t kWsRouteExtra = 100;
 constexpr size_t kWsHeader = FTMOE_WS_ZERO_BYTES;
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 

@@ -18,6 +18,7 @@
 #include "prefill.cuh"
 #include "prefill8.cuh"
 #include "route.cuh"
+#include "route_tc.cuh"
 
 using namespace ftmoe;
 
@@ -89,8 +90,19 @@ constexpr int kMaxT = 1 << 20;
 inline int cdiv(long long a, long long b) { return int((a + b - 1) / b); }
 
 // --- workspace layouts -------------------------------------------------------
+// The tensor-core router (route_tc.cuh) takes long batches of renormalised routers of 16..256
+// experts (a multiple of 16) and d <= 4096; it needs the logits in the workspace.
+bool route_tc_ok(const ftmoe_layer_desc* d, int T) {
+  return T >= FTMOE_PREFILL_MIN_T && d->renorm == 1 && d->E >= 16 && d->E <= 256 && d->E % 16 == 0 && d->d <= 4096;
+}
+// header | logits [T][E] | (tensor-core router) expert norms [E] | fallback tokens [T]
 size_t route_ws(const ftmoe_layer_desc* d, int T, bool own_logits) {
-  return kWsHeader + (own_logits ? align256(size_t(T) * d->E * sizeof(float)) : 0);
+  size_t n = kWsHeader;
+  if (own_logits) {
+    n += align256(size_t(T) * d->E * sizeof(float));
+    if (route_tc_ok(d, T)) n += align256(size_t(d->E) * 4) + align256(size_t(T) * 4);
+  }
+  return n;
 }
 size_t permute_ws(const ftmoe_layer_desc* d, int T) {
   const int P = T * d->k;
@@ -235,9 +247,11 @@ bool make_map(CUtensorMap* m, const void* base, size_t row_bytes, size_t rows, i
 bool route_can_permute(const ftmoe_layer_desc* d, int T) {
   return T <= kSelectSmallT && T * d->k <= kPermChunk;
 }
+// tc: the logits are scratch (the caller does not read them), so the tensor-core router may
+// take the call; its norms and fallback list follow the logits in the workspace.
 ftmoe_status route_impl(const ftmoe_layer_desc* d, const uint16_t* x, const uint16_t* wr, const float* bias, int T,
                         int32_t* ids, float* w, float* logits, void* ws, cudaStream_t st, int32_t* perm_off = nullptr,
-                        int32_t* perm_sp = nullptr, int32_t* perm_pp = nullptr) {
+                        int32_t* perm_sp = nullptr, int32_t* perm_pp = nullptr, bool tc = false) {
   RouteArgs a;
   const bool fp = perm_off && route_can_permute(d, T);
   a.perm_off = fp ? perm_off : nullptr;
@@ -260,6 +274,42 @@ ftmoe_status route_impl(const ftmoe_layer_desc* d, const uint16_t* x, const uint
   const int sms = num_sms();
   ftmoe_status s;
   dim3 blk(kRouteWarps * 32);
+  if (tc && route_tc_ok(d, T) && encode_tiled()) {
+    RtcArgs r;
+    r.x = x;
+    r.wr = wr;
+    r.bias = bias;
+    r.T = T;
+    r.E = d->E;
+    r.d = d->d;
+    r.k = d->k;
+    r.logits = a.logits;
+    char* extra = reinterpret_cast<char*>(a.logits) + align256(size_t(T) * d->E * sizeof(float));
+    r.wnorm = reinterpret_cast<float*>(extra);
+    r.fb_list = reinterpret_cast<int32_t*>(extra + align256(size_t(d->E) * 4));
+    r.fb_count = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kWsRouteFallback);
+    r.extra_count = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kWsRouteExtra);
+    r.ids = ids;
+    r.w = w;
+    CUtensorMap tmX, tmW;
+    if (!make_map(&tmX, x, size_t(d->d) * 2, size_t(T), kTileM) || !make_map(&tmW, wr, size_t(d->d) * 2, size_t(d->E), d->E))
+      return FTMOE_ERR_CUDA;
+    s = launch(rtc_prep_kernel, dim3(std::max(1, std::min(cdiv(d->E, 8), sms))), dim3(256), 0, st, r);
+    if (s != FTMOE_OK) return s;
+    const int tiles = cdiv(T, kTileM);
+    s = launch(rtc_logits_kernel, dim3(std::min(tiles, sms)), dim3(kRtcThreads), size_t(rtc_smem(d->E)), st, tmX, tmW,
+               r, d->E);
+    if (s != FTMOE_OK) return s;
+    const dim3 sg(std::min(cdiv(T, 8), sms * 4));
+    if (d->d <= 2048)
+      s = d->E <= 128 ? launch(rtc_select_kernel<8, 4>, sg, dim3(256), 0, st, r)
+                      : launch(rtc_select_kernel<8, 8>, sg, dim3(256), 0, st, r);
+    else
+      s = d->E <= 128 ? launch(rtc_select_kernel<16, 4>, sg, dim3(256), 0, st, r)
+                      : launch(rtc_select_kernel<16, 8>, sg, dim3(256), 0, st, r);
+    if (s != FTMOE_OK) return s;
+    return launch(rtc_fallback_kernel, dim3(sms), dim3(256), 0, st, r);
+  }
   if (T == 1) {
     const int items = d->E;
     s = launch(route_logits_kernel<1, 1, 8>, dim3(std::min(cdiv(items, kRouteWarps), sms * 8)), blk, psm, st, a,
@@ -736,7 +786,8 @@ ftmoe_status ftmoe_route(const ftmoe_layer_desc* d, const uint16_t* x, const uin
   if (!desc_ok(d) || T < 1 || T > kMaxT || !x || !wr || !ids || !w || !ws) return FTMOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(wr)) return FTMOE_ERR_INVALID_ARG;
   if (ws_bytes < route_ws(d, T, logits == nullptr)) return FTMOE_ERR_WORKSPACE;
-  return route_impl(d, x, wr, bias, T, ids, w, logits, ws, as_stream(stream));
+  return route_impl(d, x, wr, bias, T, ids, w, logits, ws, as_stream(stream), nullptr, nullptr, nullptr,
+                    logits == nullptr);
 }
 
 size_t ftmoe_permute_workspace_size(const ftmoe_layer_desc* d, int T) {
@@ -1209,7 +1260,7 @@ ftmoe_status ftmoe_layer_forward(const ftmoe_layer_desc* d, const ftmoe_weights*
                                  : layer_fused_launch<FTMOE_MXFP4>(a, r, base, st);
   }
   // route: logits go to the scratch region (the view's buffer area)
-  s = route_impl(d, x, wr, bias, T, ids_, w_, reinterpret_cast<float*>(base + L.scratch), base, st, off, sp, pp);
+  s = route_impl(d, x, wr, bias, T, ids_, w_, reinterpret_cast<float*>(base + L.scratch), base, st, off, sp, pp, true);
   if (s != FTMOE_OK) return s;
   // permute: fused into the router for small batches; else its histogram lives in the scratch region too
   if (!route_can_permute(d, T)) {
