@@ -416,7 +416,7 @@ template <int MODE, int NH>
 ftmoe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb0, const CUtensorMap& tb1, const GemmArgs& g,
                          int max_tiles, cudaStream_t st) {
   const int grid = std::max(1, std::min(num_sms(), max_tiles));
-  return launch(gemm_kernel<MODE, NH>, dim3(grid), dim3(kGemmThreads), size_t(GemmCfg<MODE, NH>::SMEM), st, ta, tb0,
+  return launch(gemm_kernel<MODE, NH>, dim3(grid), dim3(kGemmNvThreads), size_t(GemmCfg<MODE, NH>::SMEM), st, ta, tb0,
                 tb1, g);
 }
 

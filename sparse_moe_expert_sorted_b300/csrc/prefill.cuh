@@ -42,8 +42,14 @@
 //               into a kStages-deep shared-memory ring
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 2-9   epilogue; warp w reads TMEM lanes 32 * (w % 4) .. + 31
+//   warps 10-13 scale writers: each stage's scale blocks, shared memory ->
+//               registers -> TMEM (tcgen05.st, one lane quarter per warp)
 // TMEM: accumulator b at column 256 b (N <= 208 columns), the scale blocks of
-// the stage in flight right after it (48 columns, two buffers alternate).
+// the stage in flight right after it (16 + 16 * SFB_ATOMS columns, two buffers
+// alternate).  Measured on B300: writing the scales with tcgen05.st from the
+// scale warps costs the MMA issuer nothing, while tcgen05.cp copies issued
+// between its MMAs serialise with them (the 8192-token gate/up GEMM spent
+// ~80 us of ~210 us on them).
 #pragma once
 #include "tc.cuh"
 #include "permute.cuh"
@@ -54,6 +60,8 @@ constexpr int kTileM = 128;
 constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = (2 + kEpiWarps) * 32;
+constexpr int kSfWarps = 4;                                  // FP4 GEMM: scale writers
+constexpr int kGemmNvThreads = (2 + kEpiWarps + kSfWarps) * 32;
 constexpr int kStageK = 256;            // FP4 elements per stage (128 bytes per row)
 constexpr int kSfBlock = 512;           // bytes of one 128-row x K=64 scale block
 
@@ -304,8 +312,12 @@ struct GemmCfg {
   static constexpr int OFF_B = OFF_A + kStages * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + kStages * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + kStages * SFA_BYTES;
-  static constexpr int OFF_BAR = OFF_SFB + kStages * SFB_BYTES;   // full[S], empty[S], tfull[2], tempty[2], done
-  static constexpr int OFF_MISC = OFF_BAR + (2 * kStages + 5) * 8;
+  // full[S], empty[S], tfull[2], tempty[2], done, sf_full[2], sf_free[2]
+  static constexpr int OFF_BAR = OFF_SFB + kStages * SFB_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + (2 * kStages + 9) * 8;
+  // TMEM columns of one stage's scales (after the accumulator): SFA 4 per K = 64 step, then
+  // SFB 4 per step and 128-row atom
+  static constexpr int SF_COLS = 16 + 16 * SFB_ATOMS;
   static constexpr int OFF_MT = OFF_MISC + 16;                     // int s_mt[1025], s_tmp[33]
   // MODE 1: per epilogue warp, its 32 rows x NH/2 columns of the tile (row stride padded by 4 floats)
   static constexpr int STG_STRIDE = NH / 2 + 4;
@@ -314,7 +326,7 @@ struct GemmCfg {
   static constexpr int SMEM = OFF_STG + STG_BYTES + 1024;        // + alignment slack
   static constexpr uint32_t IDESC = idesc_mxf4(kTileM, N, 0);
   static_assert(N % 16 == 0 && N <= 256, "MMA N");
-  static_assert(N + 48 <= 256, "accumulator + scale columns must fit 256 TMEM columns");
+  static_assert(N + 16 + 16 * ((N + 127) / 128) <= 256, "accumulator + scale columns must fit 256 TMEM columns");
   static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1024-byte aligned stage buffers");
   static_assert(SMEM <= 232448, "one CTA's opt-in shared memory");
   static_assert(STAGE_TX < (1 << 20), "an mbarrier's transaction count");
@@ -322,7 +334,7 @@ struct GemmCfg {
 };
 
 template <int MODE, int NH>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmNvThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
             const __grid_constant__ CUtensorMap tmB1, GemmArgs a) {
   using Cfg = GemmCfg<MODE, NH>;
@@ -332,6 +344,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar_full = sb + Cfg::OFF_BAR, bar_empty = bar_full + 8 * kStages;
   const uint32_t bar_tfull = bar_empty + 8 * kStages, bar_tempty = bar_tfull + 16, bar_done = bar_tempty + 16;
+  const uint32_t bar_sffull = bar_done + 8, bar_sffree = bar_sffull + 16;
   uint32_t* s_tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
   int* s_mt = reinterpret_cast<int*>(smem + Cfg::OFF_MT);
@@ -346,6 +359,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
       mbar_init(bar_tempty + 8 * b, kEpiWarps);
+      mbar_init(bar_sffull + 8 * b, kSfWarps);
+      mbar_init(bar_sffree + 8 * b, 1);
     }
     mbar_init(bar_done, 1);
     *s_abort = 0;
@@ -412,31 +427,29 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      uint32_t stage = 0, ph = 0, acc = 0, aph = 0, sfbuf = 0;
+      uint32_t stage = 0, ph = 0, acc = 0, aph = 0, sfbuf = 0, sfph = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
         if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1, s_abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem + acc * 256;
         for (int ks = 0; ks < KS; ++ks) {
-          if (!mbar_wait(bar_full + 8 * stage, ph, s_abort)) { ok = false; break; }
+          if (!mbar_wait(bar_full + 8 * stage, ph, s_abort) || !mbar_wait(bar_sffull + 8 * sfbuf, sfph, s_abort)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const uint32_t sA = sb + Cfg::OFF_A + stage * Cfg::A_BYTES;
           const uint32_t sB = sb + Cfg::OFF_B + stage * Cfg::B_BYTES;
-          const uint32_t sSFA = sb + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES;
-          const uint32_t sSFB = sb + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES;
-          const uint32_t sf_col = tmem + sfbuf * 256 + N;    // SFA: +0..15, SFB: +16..47
+          const uint32_t sf_col = tmem + sfbuf * 256 + N;    // written by the scale warps
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            tc_cp_sf(sf_col + 4 * kk, desc_sf(sSFA + kk * kSfBlock));
-#pragma unroll
-            for (int at = 0; at < Cfg::SFB_ATOMS; ++at)
-              tc_cp_sf(sf_col + 16 + 8 * kk + 4 * at, desc_sf(sSFB + (kk * Cfg::SFB_ATOMS + at) * kSfBlock));
+          for (int kk = 0; kk < 4; ++kk)
             mma_nvf4(d_tmem, desc_sw128(sA + 32 * kk), desc_sw128(sB + 32 * kk), Cfg::IDESC, sf_col + 4 * kk,
-                     sf_col + 16 + 8 * kk, (ks | kk) != 0);
-          }
+                     sf_col + 16 + 4 * Cfg::SFB_ATOMS * kk, (ks | kk) != 0);
           tc_commit(bar_empty + 8 * stage);
+          tc_commit(bar_sffree + 8 * sfbuf);
           sfbuf ^= 1;
+          if (sfbuf == 0) sfph ^= 1;
           if (++stage == kStages) { stage = 0; ph ^= 1; }
         }
         if (!ok) break;
@@ -452,6 +465,55 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       tc_commit(bar_done);
       mbar_wait(bar_done, 0, nullptr);
     }
+  } else if (warp >= 2 + kEpiWarps) {
+    // ---------------- scale writers ----------------
+    // Lane l of the warp of quarter q writes TMEM lane 32 q + l: in every quarter, column
+    // c of a K = 64 step holds bytes 16 l + 4 c .. + 3 of the step's 512-byte scale block
+    // (the scales of row 32 c + l), the layout the block-scaled MMA reads.
+    const int q = warp & 3;
+    const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16) + N;
+    uint32_t stage = 0, ph = 0, sfbuf = 0, sfph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int ks = 0; ks < KS; ++ks) {
+        if (!mbar_wait_warp(bar_full + 8 * stage, ph, s_abort) ||
+            !mbar_wait_warp(bar_sffree + 8 * sfbuf, sfph ^ 1, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint4* sfa = reinterpret_cast<const uint4*>(smem + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES) + lane;
+        const uint4* sfb = reinterpret_cast<const uint4*>(smem + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES) + lane;
+        uint32_t v[16];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint4 w = sfa[kk * (kSfBlock / 16)];
+          v[4 * kk] = w.x; v[4 * kk + 1] = w.y; v[4 * kk + 2] = w.z; v[4 * kk + 3] = w.w;
+        }
+        const uint32_t col = lane_base + sfbuf * 256;
+        tc_st16(col, v);
+#pragma unroll
+        for (int h = 0; h < Cfg::SFB_ATOMS; ++h) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {      // blocks 4h .. 4h + 3 in (kk, atom) order
+            const uint4 w = sfb[(4 * h + i) * (kSfBlock / 16)];
+            v[4 * i] = w.x; v[4 * i + 1] = w.y; v[4 * i + 2] = w.z; v[4 * i + 3] = w.w;
+          }
+          tc_st16(col + 16 + 16 * h, v);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sffull + 8 * sfbuf);
+        sfbuf ^= 1;
+        if (sfbuf == 0) sfph ^= 1;
+        if (++stage == kStages) { stage = 0; ph ^= 1; }
+      }
+    }
+    if (!ok && lane == 0) {
+      set_dev_err(DEV_ERR_TIMEOUT);
+      *s_abort = 1;
+    }
   } else {
     // ---------------- epilogue ----------------
     const int q = warp & 3;             // TMEM lane quarter of this warp
@@ -462,6 +524,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       const int mt = tile / NT, nt = tile % NT;
       const int e = expert_of_mtile(s_mt, a.E, mt);
       const int slot = a.slot_of ? a.slot_of[e] : e;
+      // tensor scales: gate and up (MODE 0), down (MODE 1); loaded before the wait
+      const float ts0 = a.tscale ? a.tscale[slot * 3 + (MODE == 0 ? 0 : 2)] : 1.f;
+      const float ts1 = (MODE == 0 && a.tscale) ? a.tscale[slot * 3 + 1] : 1.f;
       if (!mbar_wait(bar_tfull + 8 * acc, aph, s_abort)) {
         if (lane == 0) {
           set_dev_err(DEV_ERR_TIMEOUT);
@@ -472,6 +537,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       tc_fence_after();
       const uint32_t tb = tmem + (uint32_t(q * 32) << 16) + acc * 256;
       const int j = mt * kTileM + r;   // padded row
+      // the accumulator goes back to the MMA issuer as soon as its values are in registers
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+      };
       if (MODE == 0) {
         constexpr int NB = NH / 32;    // 16-column blocks per warp
         uint32_t g[NB][16], u[NB][16];
@@ -486,8 +557,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           tc_reg_fence(g[b]);
           tc_reg_fence(u[b]);
         }
-        const float tsg = a.tscale ? a.tscale[slot * 3 + 0] : 1.f;
-        const float tsu = a.tscale ? a.tscale[slot * 3 + 1] : 1.f;
+        release();
+        const float tsg = ts0, tsu = ts1;
         const int fsteps = a.f / 64;
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
@@ -513,10 +584,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         tc_wait_ld();
 #pragma unroll
         for (int b = 0; b < NB; ++b) tc_reg_fence(v[b]);
+        release();
         const int lo = a.offsets[e];
         const int i = j - s_mt[e] * kTileM;
         if (i < a.offsets[e + 1] - lo) {
-          const float tsd = a.tscale ? a.tscale[slot * 3 + 2] : 1.f;
+          const float tsd = ts0;
           float* dst = a.out + size_t(lo + i) * a.d + nt * NH + half * (NH / 2);
 #pragma unroll
           for (int b = 0; b < NB; ++b)
@@ -541,7 +613,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           const int p = a.sorted_pair[lo + i];
           if (p >= 0 && p < a.P) {
             tok = p / a.k;
-            w = a.topk_w[p] * (a.tscale ? a.tscale[slot * 3 + 2] : 1.f);
+            w = a.topk_w[p] * ts0;
           } else {
             set_dev_err(DEV_ERR_BAD_PAIR);
           }
@@ -552,6 +624,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         tc_wait_ld();
 #pragma unroll
         for (int b = 0; b < NB; ++b) tc_reg_fence(v[b]);
+        release();
         float* my = stg + lane * Cfg::STG_STRIDE;
 #pragma unroll
         for (int b = 0; b < NB; ++b)
@@ -574,9 +647,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
         __syncwarp();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
       acc ^= 1;
       if (acc == 0) aph ^= 1;
     }
