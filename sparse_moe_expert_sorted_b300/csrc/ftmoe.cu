@@ -139,8 +139,9 @@ size_t tc_rows_cap(const ftmoe_layer_desc* d, int T) {
 }
 
 // header | xq_tok [T][d/2] | sf_tok [T][d/16] | xq [R][d/2] | sfa [R][d/16] | hq [R][f/2] | sfh [R][f/16]
+//        | rowmeta [R] int4
 struct TcWs {
-  size_t rows, xq_tok, sf_tok, xq, sfa, hq, sfh, total;
+  size_t rows, xq_tok, sf_tok, xq, sfa, hq, sfh, rowmeta, total;
 };
 TcWs tc_ws(const ftmoe_layer_desc* d, int T) {
   TcWs w;
@@ -152,13 +153,15 @@ TcWs tc_ws(const ftmoe_layer_desc* d, int T) {
   w.sfa = o; o += align1k(w.rows * d->d / 16);
   w.hq = o; o += align1k(w.rows * d->ffn / 2);
   w.sfh = o; o += align1k(w.rows * d->ffn / 16);
+  w.rowmeta = o; o += align1k(w.rows * 16);
   w.total = o;
   return w;
 }
 
 // FP8 path: header | xq_tok [T][d] | sx_tok [T][d/128] | xq [R][d] | sx [d/128][R] | hq [R][f] | sh [f/128][R]
+//           | rowmeta [R] int4
 struct Tc8Ws {
-  size_t rows, xq_tok, sx_tok, xq, sx, hq, sh, total;
+  size_t rows, xq_tok, sx_tok, xq, sx, hq, sh, rowmeta, total;
 };
 Tc8Ws tc8_ws(const ftmoe_layer_desc* d, int T) {
   Tc8Ws w;
@@ -170,6 +173,7 @@ Tc8Ws tc8_ws(const ftmoe_layer_desc* d, int T) {
   w.sx = o; o += align1k(w.rows * (d->d / 128) * 4);
   w.hq = o; o += align1k(w.rows * d->ffn);
   w.sh = o; o += align1k(w.rows * (d->ffn / 128) * 4);
+  w.rowmeta = o; o += align1k(w.rows * 16);
   w.total = o;
   return w;
 }
@@ -458,6 +462,8 @@ ftmoe_status ffn_tc_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, cons
   q.rows_cap = int(L.rows);
   q.zero_out = reinterpret_cast<float4*>(zero_out);
   q.zero_n4 = zero_out ? (long long)T * d->d / 4 : 0;
+  q.topk_w = topk_w;
+  q.rowmeta = reinterpret_cast<int4*>(base + L.rowmeta);
   s = launch(actq_gather_kernel, dim3(std::min(cdiv(L.rows, kActqWarps), sms * 8)),
                           dim3(kActqWarps * 32), 0, st, q);
   if (s != FTMOE_OK) return s;
@@ -498,6 +504,7 @@ ftmoe_status ffn_tc_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, cons
   g.sfh = nullptr;
   g.topk_w = topk_w;
   g.out = y_or_out;
+  g.rowmeta = reinterpret_cast<const int4*>(base + L.rowmeta);
   return launch_gemm<1, 128>(tA2, tD, tD, g, mts * (d->d / 128), st);
 }
 
@@ -548,6 +555,8 @@ ftmoe_status ffn_tc8_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, con
   q.rows_cap = int(L.rows);
   q.zero_out = reinterpret_cast<float4*>(zero_out);
   q.zero_n4 = zero_out ? (long long)T * d->d / 4 : 0;
+  q.topk_w = topk_w;
+  q.rowmeta = reinterpret_cast<int4*>(base + L.rowmeta);
   s = launch(gather8_kernel, dim3(std::min(cdiv(L.rows, kActqWarps), sms * 8)), dim3(kActqWarps * 32), 0, st, q);
   if (s != FTMOE_OK) return s;
   CUtensorMap tA1, tG, tU, tA2, tD;
@@ -584,6 +593,7 @@ ftmoe_status ffn_tc8_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, con
   g.sh = nullptr;
   g.topk_w = topk_w;
   g.out = y_or_out;
+  g.rowmeta = reinterpret_cast<const int4*>(base + L.rowmeta);
   return launch_gemm8<1>(tA2, tD, tD, g, mts * (d->d / 256), st);
 }
 

@@ -162,7 +162,17 @@ struct ActqArgs {
   int rows_cap;
   float4* zero_out;   // optional: zeroed first (T*d/4 float4)
   long long zero_n4;
+  const float* topk_w;   // or nullptr
+  int4* rowmeta;         // [rows_cap] per padded row (row_meta)
 };
+
+// Per padded row, for the down GEMM's epilogue: {sorted index of the pair or -1, token or -1,
+// the pair's combine weight (fp32 bits; 0 without topk_w), 0}.  Written by the gather kernel,
+// which reads the sorted pairs anyway, so the epilogue needs one load per row instead of a
+// chain of three (offsets -> sorted pair -> weight).
+__device__ __forceinline__ int4 row_meta(int yrow, int p, int k, const float* topk_w) {
+  return make_int4(yrow, p >= 0 ? p / k : -1, (p >= 0 && topk_w) ? __float_as_int(topk_w[p]) : 0, 0);
+}
 
 constexpr int kActqWarps = 8;
 
@@ -191,6 +201,9 @@ __global__ void __launch_bounds__(kActqWarps * 32) actq_gather_kernel(ActqArgs a
       const int p = a.sorted_pair[lo + i];
       if (p >= 0 && p < a.P) tok = p / a.k;
       else set_dev_err(DEV_ERR_BAD_PAIR);
+      if (lane == 0) a.rowmeta[j] = row_meta(lo + i, tok >= 0 ? p : -1, a.k, a.topk_w);
+    } else if (lane == 0) {
+      a.rowmeta[j] = make_int4(-1, -1, 0, 0);
     }
     const uint8_t* qs = a.xq_tok + size_t(tok < 0 ? 0 : tok) * (a.d / 2);
     const uint8_t* ss = a.sf_tok + size_t(tok < 0 ? 0 : tok) * nb;
@@ -297,6 +310,7 @@ struct GemmArgs {
   uint8_t* sfh;             // MODE 0: h scale blocks [rows_cap/128][f/64][512]
   const float* topk_w;      // MODE 1: fused combine weights, or nullptr (write y)
   float* out;               // MODE 1: out [T][d] (fused) or y [P][d] (sorted)
+  const int4* rowmeta;      // MODE 1: row_meta of each padded row
 };
 
 template <int MODE, int NH>
@@ -527,6 +541,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       // tensor scales: gate and up (MODE 0), down (MODE 1); loaded before the wait
       const float ts0 = a.tscale ? a.tscale[slot * 3 + (MODE == 0 ? 0 : 2)] : 1.f;
       const float ts1 = (MODE == 0 && a.tscale) ? a.tscale[slot * 3 + 1] : 1.f;
+      const int j = mt * kTileM + r;   // padded row
+      const int4 meta = MODE == 1 ? __ldg(a.rowmeta + j) : make_int4(-1, -1, 0, 0);
       if (!mbar_wait(bar_tfull + 8 * acc, aph, s_abort)) {
         if (lane == 0) {
           set_dev_err(DEV_ERR_TIMEOUT);
@@ -536,7 +552,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       }
       tc_fence_after();
       const uint32_t tb = tmem + (uint32_t(q * 32) << 16) + acc * 256;
-      const int j = mt * kTileM + r;   // padded row
       // the accumulator goes back to the MMA issuer as soon as its values are in registers
       auto release = [&]() {
         tc_fence_before();
@@ -585,11 +600,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
         for (int b = 0; b < NB; ++b) tc_reg_fence(v[b]);
         release();
-        const int lo = a.offsets[e];
-        const int i = j - s_mt[e] * kTileM;
-        if (i < a.offsets[e + 1] - lo) {
+        if (meta.x >= 0) {
           const float tsd = ts0;
-          float* dst = a.out + size_t(lo + i) * a.d + nt * NH + half * (NH / 2);
+          float* dst = a.out + size_t(meta.x) * a.d + nt * NH + half * (NH / 2);
 #pragma unroll
           for (int b = 0; b < NB; ++b)
 #pragma unroll
@@ -605,19 +618,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         constexpr int NB = NH / 32;
         constexpr int HC = NH / 2;                  // columns of this warp
         float* stg = reinterpret_cast<float*>(smem + Cfg::OFF_STG) + (warp - 2) * 32 * Cfg::STG_STRIDE;
-        const int lo = a.offsets[e];
-        const int i = j - s_mt[e] * kTileM;
-        int tok = -1;
-        float w = 0.f;
-        if (i < a.offsets[e + 1] - lo) {
-          const int p = a.sorted_pair[lo + i];
-          if (p >= 0 && p < a.P) {
-            tok = p / a.k;
-            w = a.topk_w[p] * ts0;
-          } else {
-            set_dev_err(DEV_ERR_BAD_PAIR);
-          }
-        }
+        const int tok = meta.y;
+        const float w = __int_as_float(meta.z) * ts0;
         uint32_t v[NB][16];
 #pragma unroll
         for (int b = 0; b < NB; ++b) tc_ld16(tb + half * HC + 16 * b, v[b]);

@@ -78,6 +78,8 @@ struct Gather8Args {
   int rows_cap;
   float4* zero_out;
   long long zero_n4;
+  const float* topk_w;     // or nullptr
+  int4* rowmeta;           // [rows_cap] row_meta of each padded row
 };
 
 __global__ void __launch_bounds__(kActqWarps * 32) gather8_kernel(Gather8Args a) {
@@ -103,6 +105,9 @@ __global__ void __launch_bounds__(kActqWarps * 32) gather8_kernel(Gather8Args a)
       const int p = a.sorted_pair[lo + i];
       if (p >= 0 && p < a.P) tok = p / a.k;
       else set_dev_err(DEV_ERR_BAD_PAIR);
+      if (lane == 0) a.rowmeta[j] = row_meta(lo + i, tok >= 0 ? p : -1, a.k, a.topk_w);
+    } else if (lane == 0) {
+      a.rowmeta[j] = make_int4(-1, -1, 0, 0);
     }
     const uint4* src = reinterpret_cast<const uint4*>(a.xq_tok + size_t(tok < 0 ? 0 : tok) * a.d);
     uint4* dst = reinterpret_cast<uint4*>(a.xq + size_t(j) * a.d);
@@ -124,6 +129,7 @@ struct Gemm8Args {
   float* sh;                // MODE 0: h scales [f/128][rows_cap]
   const float* topk_w;      // MODE 1: fused combine weights, or nullptr (write y)
   float* out;               // MODE 1: out [T][d] (fused) or y [P][d] (sorted)
+  const int4* rowmeta;      // MODE 1: row_meta of each padded row
 };
 
 template <int MODE>
@@ -282,6 +288,7 @@ gemm8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       const int e = expert_of_mtile(s_mt, a.E, mt);
       const int slot = a.slot_of ? a.slot_of[e] : e;
       const int j = mt * kTileM + r;
+      const int4 meta = MODE == 1 ? __ldg(a.rowmeta + j) : make_int4(-1, -1, 0, 0);   // used after the K loop
       // the tile's weight block scales (two 128-column blocks x KS steps)
       g8_epi_sync();
       for (int i = et; i < 2 * KS; i += kEpiWarps * 32) {
@@ -365,23 +372,11 @@ gemm8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         }
         if (half == 0) a.sh[size_t(nt) * a.rows_cap + j] = s;
       } else if (ok) {
-        const int lo = a.offsets[e];
-        const int i = j - s_mt[e] * kTileM;
-        const bool valid = i < a.offsets[e + 1] - lo;
         if (a.topk_w) {
           // fused combine: stage w * y (32 rows x 32 columns at a time), add row by row
           float* stg = reinterpret_cast<float*>(smem + Cfg::OFF_STG) + (warp - 2) * 32 * Cfg::STG_W;
-          int tok = -1;
-          float w = 0.f;
-          if (valid) {
-            const int p = a.sorted_pair[lo + i];
-            if (p >= 0 && p < a.P) {
-              tok = p / a.k;
-              w = a.topk_w[p];
-            } else {
-              set_dev_err(DEV_ERR_BAD_PAIR);
-            }
-          }
+          const int tok = meta.y;
+          const float w = __int_as_float(meta.z);
 #pragma unroll
           for (int b = 0; b < 2; ++b)
 #pragma unroll
@@ -404,8 +399,8 @@ gemm8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
               }
               __syncwarp();
             }
-        } else if (valid) {
-          float* dst = a.out + size_t(lo + i) * a.d + nt * 256 + half * 64;
+        } else if (meta.x >= 0) {
+          float* dst = a.out + size_t(meta.x) * a.d + nt * 256 + half * 64;
 #pragma unroll
           for (int b = 0; b < 2; ++b)
 #pragma unroll
