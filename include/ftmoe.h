@@ -116,7 +116,7 @@ typedef struct {
  *   1. Prefill (NVFP4, d and ffn multiples of 256): the weight block scales
  *      repacked for the tensor-core path.  Each MMA with K = 64 reads four scales
  *      per row from tensor memory; per 128 weight rows and per K = 64 step the
- *      layout holds the 512 bytes that one tcgen05.cp moves there: byte
+ *      layout holds the 512 bytes that fill four tensor-memory columns there: byte
  *      (r % 32) * 16 + (r / 32) * 4 + kb for row r of the 128 and 16-element
  *      block kb of the 64.  The tensor-core path reads the codes in place.
  *        gate/up  [C][ffn/NH][d/64][A][512]: an N tile of NH gate rows then NH up
@@ -175,7 +175,7 @@ ftmoe_status ftmoe_prepare_weights(const ftmoe_layer_desc* desc, const ftmoe_wei
  * k-th value; their logits are recomputed in order R and the top-k taken from
  * them, so ids and weights equal those above bit for bit.  Tokens with more
  * than 32 candidates are recomputed entirely in order R.  The workspace's
- * uint32 at byte 96 then counts those tokens, and the uint32 at byte 100 the
+ * uint32 at byte 128 then counts those tokens, and the uint32 at byte 132 the
  * tokens with more than k candidates.
  * Preconditions: 1 <= T <= 2^20, d % 256 == 0.
  * ------------------------------------------------------------------------- */

@@ -47,13 +47,15 @@ constexpr size_t kWsBarrierGen = 20;      // uint32: grid barrier generation (on
 // uint64: arrivals of the grid syncs of kernels whose grid is exactly one CTA per SM.  Only
 // ever incremented, so it stays a multiple of that grid size between syncs.
 constexpr size_t kWsGridSync = 24;
-// uint32 [8]: per output slice, the clusters that have added their partial (the cluster form
-// of the one-kernel decode layer; the last one sums and sets it back to 0).
+// uint32 [16]: per output slice, the clusters that have added their partial (the cluster form
+// of the one-kernel decode layer, clusters of up to 16 CTAs; the last one sums and sets it
+// back to 0).
 constexpr size_t kWsClusterCnt = 64;
+constexpr int kMaxClusterSize = 16;
 // uint32: tokens the tensor-core router left to its full order-R fallback, and tokens for which
 // it recomputed more than k logits in order R (both set by each such call).
-constexpr size_t kWsRouteFallback = 96;
-constexpr size_t kWsRouteExtra = 100;
+constexpr size_t kWsRouteFallback = 128;
+constexpr size_t kWsRouteExtra = 132;
 constexpr size_t kWsHeader = FTMOE_WS_ZERO_BYTES;
 static inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 

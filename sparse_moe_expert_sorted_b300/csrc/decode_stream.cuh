@@ -1861,12 +1861,13 @@ tail:
     const uint32_t part0 = smem_u32(sm);
     float* cpart = ra.part + size_t(cid) * n;
     for (int o = lo + tid; o < hi; o += kSdThreads) {
-      float pv[8];   // the cluster's partials of output o, loaded together, added in rank order
+      float pv[kMaxClusterSize];   // the cluster's partials of output o, loaded together, added in rank order
 #pragma unroll
-      for (int q = 0; q < 8; ++q) pv[q] = q < csz ? ld_cluster_f32(mapa_shared(part0 + 4u * uint32_t(o), uint32_t(q))) : 0.f;
+      for (int q = 0; q < kMaxClusterSize; ++q)
+        pv[q] = q < csz ? ld_cluster_f32(mapa_shared(part0 + 4u * uint32_t(o), uint32_t(q))) : 0.f;
       float v = 0.f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
+      for (int q = 0; q < kMaxClusterSize; ++q)
         if (q < csz) v += pv[q];
       cpart[o] = v;
     }

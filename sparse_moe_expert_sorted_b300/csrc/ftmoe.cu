@@ -1105,8 +1105,16 @@ SlClusterPlan sl_cluster_plan(const FfnArgs& a, const SlLayout& Ls) {
   if (it != cache.end()) return it->second;
   SlClusterPlan plan{0, 0};
   auto kern = sl_layer_kernel<FMT, NCOL, true>;
-  if (resident_ctas(kern, kSdThreads, size_t(Ls.smem)) >= 1) {
-    for (int cs : {8, 4, 2}) {
+  // Each CTA streams the router rows of E / cs experts before the selection (measured on
+  // B300: ~2.9 us for 128 KB per SM), and the FFN items spread over the grid (~1.5 us per
+  // item of a d 2048, ffn 768 NVFP4 expert).  The plan takes the cluster size with the least
+  // estimated time of the two; 16 needs the non-portable cluster attribute.
+  const double us_per_row_byte = 2.9 / (128.0 * 1024.0), us_per_item = 1.5;
+  const long long items = (long long)std::min(a.E, a.T * a.k) * (a.f / kSdRowsA);
+  double best = 1e30;
+  if (resident_ctas(kern, kSdThreads, size_t(Ls.smem)) >= 1 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    for (int cs : {16, 8, 4, 2}) {
       const long long epc = (a.E + cs - 1) / cs;
       if (epc * a.d * 2 > (long long)Ls.stages * Ls.stage_bytes || num_sms() < cs) continue;
       cudaLaunchConfig_t cfg = {};
@@ -1126,9 +1134,15 @@ SlClusterPlan sl_cluster_plan(const FfnArgs& a, const SlLayout& Ls) {
         continue;
       }
       const int grid = std::min(n, num_sms() / cs) * cs;
-      if (n >= 1 && grid > plan.grid) plan = SlClusterPlan{cs, grid};
+      if (n < 1) continue;
+      const double est = double(epc) * a.d * 2 * us_per_row_byte + double((items + grid - 1) / grid) * us_per_item;
+      if (est < best) {
+        best = est;
+        plan = SlClusterPlan{cs, grid};
+      }
     }
   }
+  (void)cudaGetLastError();
   cache[key] = plan;
   return plan;
 }

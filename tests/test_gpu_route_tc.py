@@ -30,8 +30,8 @@ from gpu_helpers import ensure_built
 from helpers import bf16_bits
 
 pytestmark = pytest.mark.gpu
-FALLBACK_WORD = 96 // 4        # the header's uint32 index of the full-fallback count
-EXTRA_WORD = 100 // 4          # ... and of the count of tokens with more than k candidates
+FALLBACK_WORD = 128 // 4       # the header's uint32 index of the full-fallback count
+EXTRA_WORD = 132 // 4          # ... and of the count of tokens with more than k candidates
 
 
 def _gamma(d):
