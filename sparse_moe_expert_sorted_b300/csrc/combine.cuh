@@ -28,6 +28,9 @@ struct CombineArgs {
 __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
   pdl_wait();
   const int q = a.d / 4;
+  // the bf16 cast of an out that already holds the sum (no y, partial_b == out_f32): out_f32
+  // is only read
+  float* out_f32 = (a.y == nullptr && a.out_f32 == a.partial_b) ? nullptr : a.out_f32;
   const long long total = (long long)a.T * q;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
@@ -54,7 +57,7 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineArgs a) {
         acc.w = fmaf(w, v.w, acc.w);
       }
     }
-    if (a.out_f32) reinterpret_cast<float4*>(a.out_f32 + size_t(t) * a.d)[c4] = acc;
+    if (out_f32) reinterpret_cast<float4*>(out_f32 + size_t(t) * a.d)[c4] = acc;
     if (a.out_bf16) {
       __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
       __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);

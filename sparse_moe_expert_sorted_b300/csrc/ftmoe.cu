@@ -464,7 +464,7 @@ ftmoe_status ffn_tc_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, cons
   q.zero_n4 = zero_out ? (long long)T * d->d / 4 : 0;
   q.topk_w = topk_w;
   q.rowmeta = reinterpret_cast<int4*>(base + L.rowmeta);
-  s = launch(actq_gather_kernel, dim3(std::min(cdiv(L.rows, kActqWarps), sms * 8)),
+  s = launch(actq_gather_kernel, dim3(std::min(cdiv(L.rows, 32 * kActqWarps), sms * 8)),
                           dim3(kActqWarps * 32), 0, st, q);
   if (s != FTMOE_OK) return s;
 

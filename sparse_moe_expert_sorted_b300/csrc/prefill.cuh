@@ -176,6 +176,9 @@ __device__ __forceinline__ int4 row_meta(int yrow, int p, int k, const float* to
 
 constexpr int kActqWarps = 8;
 
+// One warp per 32 consecutive padded rows: lane i first resolves row j0 + i (expert, sorted
+// pair, token) so the warp pays the chain of dependent loads once per 32 rows, writes the row's
+// metadata and its scale words, then the warp copies the 32 rows' codes 16 bytes per lane.
 __global__ void __launch_bounds__(kActqWarps * 32) actq_gather_kernel(ActqArgs a) {
   __shared__ int s_mt[1025];
   __shared__ int s_tmp[33];
@@ -188,42 +191,65 @@ __global__ void __launch_bounds__(kActqWarps * 32) actq_gather_kernel(ActqArgs a
   }
   const int MT = build_mtile_starts(a.offsets, a.slot_of, a.E, a.C, a.rows_cap / kTileM, s_mt, s_tmp);
   const int lane = threadIdx.x & 31;
-  const int nb = a.d / 16;           // 16-element blocks per row (multiple of 16)
-  const int ksteps = a.d / 64;
-  const int rows = MT * kTileM;
-  for (int j = blockIdx.x * kActqWarps + (threadIdx.x >> 5); j < rows; j += gridDim.x * kActqWarps) {
-    const int mt = j / kTileM;
-    const int e = expert_of_mtile(s_mt, a.E, mt);
+  const int nb = a.d / 16;           // scale bytes per row
+  const int ksteps = a.d / 64;       // scale words per row
+  const int row_bytes = a.d / 2;
+  const int n16 = row_bytes / 16;    // 16-byte pieces of a row's codes
+  const int rows = MT * kTileM;      // a multiple of 32
+  for (int j0 = (blockIdx.x * kActqWarps + (threadIdx.x >> 5)) * 32; j0 < rows; j0 += gridDim.x * kActqWarps * 32) {
+    const int j = j0 + lane;
+    const int e = expert_of_mtile(s_mt, a.E, j / kTileM);
     const int i = j - s_mt[e] * kTileM;
     const int lo = a.offsets[e];
     int tok = -1;
+    int4 meta = make_int4(-1, -1, 0, 0);
     if (i < a.offsets[e + 1] - lo) {
-      const int p = a.sorted_pair[lo + i];
-      if (p >= 0 && p < a.P) tok = p / a.k;
-      else set_dev_err(DEV_ERR_BAD_PAIR);
-      if (lane == 0) a.rowmeta[j] = row_meta(lo + i, tok >= 0 ? p : -1, a.k, a.topk_w);
-    } else if (lane == 0) {
-      a.rowmeta[j] = make_int4(-1, -1, 0, 0);
-    }
-    const uint8_t* qs = a.xq_tok + size_t(tok < 0 ? 0 : tok) * (a.d / 2);
-    const uint8_t* ss = a.sf_tok + size_t(tok < 0 ? 0 : tok) * nb;
-    uint8_t* qr = a.xq + size_t(j) * (a.d / 2);
-    for (int base = 0; base < nb; base += 32) {
-      const int b = base + lane;
-      uint2 c = make_uint2(0u, 0u);
-      uint32_t sc = 0;
-      if (b < nb && tok >= 0) {
-        c = __ldg(reinterpret_cast<const uint2*>(qs) + b);
-        sc = __ldg(ss + b);
+      int p = a.sorted_pair[lo + i];
+      if (p >= 0 && p < a.P) {
+        tok = p / a.k;
+      } else {
+        set_dev_err(DEV_ERR_BAD_PAIR);
+        p = -1;
       }
-      if (b < nb) reinterpret_cast<uint2*>(qr)[b] = c;
-      // lanes 4g..4g+3 hold the four scale bytes of one K = 64 step: one 32-bit store
-      uint32_t word = sc;
-      word |= __shfl_down_sync(0xFFFFFFFFu, sc, 1) << 8;
-      word |= __shfl_down_sync(0xFFFFFFFFu, sc, 2) << 16;
-      word |= __shfl_down_sync(0xFFFFFFFFu, sc, 3) << 24;
-      if (b < nb && (lane & 3) == 0)
-        *reinterpret_cast<uint32_t*>(a.sfa + sf_offset(j, b, ksteps)) = word;
+      meta = row_meta(lo + i, p, a.k, a.topk_w);
+    }
+    a.rowmeta[j] = meta;
+    // scale words of row j: the four E4M3 scales of K = 64 step ks (little-endian) go to byte
+    // (r % 32) * 16 + (r / 32) * 4 of the step's 512-byte block
+    {
+      const uint32_t* ss = reinterpret_cast<const uint32_t*>(a.sf_tok + size_t(tok < 0 ? 0 : tok) * nb);
+      const int r = j & (kTileM - 1);
+      uint8_t* blk = a.sfa + size_t(j / kTileM) * ksteps * kSfBlock + (r & 31) * 16 + (r >> 5) * 4;
+#pragma unroll 8
+      for (int ks = 0; ks < ksteps; ++ks)
+        *reinterpret_cast<uint32_t*>(blk + size_t(ks) * kSfBlock) = tok >= 0 ? __ldg(ss + ks) : 0u;
+    }
+    // codes of the 32 rows, four rows' loads in flight at a time
+    for (int r0 = 0; r0 < 32; r0 += 4) {
+      int tr[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tr[q] = __shfl_sync(0xFFFFFFFFu, tok, r0 + q);
+      for (int c0 = 0; c0 < n16; c0 += 64) {
+        uint4 v[4][2];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.xq_tok + size_t(tr[q] < 0 ? 0 : tr[q]) * row_bytes);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = c0 + 32 * h + lane;
+            v[q][h] = (tr[q] >= 0 && c < n16) ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4* dst = reinterpret_cast<uint4*>(a.xq + size_t(j0 + r0 + q) * row_bytes);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int c = c0 + 32 * h + lane;
+            if (c < n16) dst[c] = v[q][h];
+          }
+        }
+      }
     }
   }
 }
