@@ -347,14 +347,15 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = 4 * kSfBlock;
   static constexpr int SFB_ATOMS = (N + 127) / 128;
   static constexpr int SFB_BYTES = 4 * SFB_ATOMS * kSfBlock;
-  static constexpr int STAGE_TX = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGE_TX = A_BYTES + B_BYTES;        // on full[s]
+  static constexpr int SF_TX = SFA_BYTES + SFB_BYTES;         // on sfld[s]
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + kStages * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + kStages * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + kStages * SFA_BYTES;
-  // full[S], empty[S], tfull[2], tempty[2], done, sf_full[2], sf_free[2]
+  // full[S], empty[S], tfull[2], tempty[2], done, sf_full[2], sf_free[2], sfld[S]
   static constexpr int OFF_BAR = OFF_SFB + kStages * SFB_BYTES;
-  static constexpr int OFF_MISC = OFF_BAR + (2 * kStages + 9) * 8;
+  static constexpr int OFF_MISC = OFF_BAR + (3 * kStages + 9) * 8;
   // TMEM columns of one stage's scales (after the accumulator): SFA 4 per K = 64 step, then
   // SFB 4 per step and 128-row atom
   static constexpr int SF_COLS = 16 + 16 * SFB_ATOMS;
@@ -384,7 +385,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar_full = sb + Cfg::OFF_BAR, bar_empty = bar_full + 8 * kStages;
   const uint32_t bar_tfull = bar_empty + 8 * kStages, bar_tempty = bar_tfull + 16, bar_done = bar_tempty + 16;
-  const uint32_t bar_sffull = bar_done + 8, bar_sffree = bar_sffull + 16;
+  const uint32_t bar_sffull = bar_done + 8, bar_sffree = bar_sffull + 16, bar_sfld = bar_sffree + 16;
   uint32_t* s_tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
   int* s_mt = reinterpret_cast<int*>(smem + Cfg::OFF_MT);
@@ -395,6 +396,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
+      mbar_init(bar_sfld + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
@@ -438,6 +440,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         const uint8_t* sfb_src = a.sfb + (size_t(slot) * NT + nt) * ksteps * Cfg::SFB_ATOMS * kSfBlock;
         for (int ks = 0; ks < KS; ++ks) {
           if (!mbar_wait(bar_empty + 8 * stage, ph ^ 1, s_abort)) { ok = false; break; }
+          // the scales first, on their own barrier: the scale warps can move them into TMEM
+          // before the (larger) A and B tiles have landed
+          const uint32_t fs = bar_sfld + 8 * stage;
+          mbar_arrive_expect_tx(fs, Cfg::SF_TX);
+          bulk_load(sb + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES, sfa_src + size_t(ks) * Cfg::SFA_BYTES,
+                    Cfg::SFA_BYTES, fs);
+          bulk_load(sb + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES, sfb_src + size_t(ks) * Cfg::SFB_BYTES,
+                    Cfg::SFB_BYTES, fs);
           const uint32_t fb = bar_full + 8 * stage;
           mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
           const uint32_t sA = sb + Cfg::OFF_A + stage * Cfg::A_BYTES;
@@ -445,10 +455,6 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           tma_load_2d(sA, &tmA, ks * 128, mt * kTileM, fb);
           tma_load_2d(sB, &tmB0, ks * 128, brow, fb);
           if (MODE == 0) tma_load_2d(sB + NH * 128, &tmB1, ks * 128, brow, fb);
-          bulk_load(sb + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES, sfa_src + size_t(ks) * Cfg::SFA_BYTES,
-                    Cfg::SFA_BYTES, fb);
-          bulk_load(sb + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES, sfb_src + size_t(ks) * Cfg::SFB_BYTES,
-                    Cfg::SFB_BYTES, fb);
           ++issued;
           if (++stage == kStages) { stage = 0; ph ^= 1; }
         }
@@ -461,6 +467,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           if (stage == 0) { stage = kStages; ph ^= 1; }
           --stage;
           mbar_wait(bar_full + 8 * stage, ph, nullptr);
+          mbar_wait(bar_sfld + 8 * stage, ph, nullptr);
         }
       }
     }
@@ -516,7 +523,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     bool ok = true;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
       for (int ks = 0; ks < KS; ++ks) {
-        if (!mbar_wait_warp(bar_full + 8 * stage, ph, s_abort) ||
+        if (!mbar_wait_warp(bar_sfld + 8 * stage, ph, s_abort) ||
             !mbar_wait_warp(bar_sffree + 8 * sfbuf, sfph ^ 1, s_abort)) {
           ok = false;
           break;
