@@ -305,12 +305,13 @@ ftmoe_status route_impl(const ftmoe_layer_desc* d, const uint16_t* x, const uint
                r, d->E);
     if (s != FTMOE_OK) return s;
     const dim3 sg(std::min(cdiv(T, 8), sms * 4));
+    const size_t xs8 = 8 * 8 * 512, xs16 = 8 * 16 * 512;   // per-warp x rows in shared memory
     if (d->d <= 2048)
-      s = d->E <= 128 ? launch(rtc_select_kernel<8, 4>, sg, dim3(256), 0, st, r)
-                      : launch(rtc_select_kernel<8, 8>, sg, dim3(256), 0, st, r);
+      s = d->E <= 128 ? launch(rtc_select_kernel<8, 4>, sg, dim3(256), xs8, st, r)
+                      : launch(rtc_select_kernel<8, 8>, sg, dim3(256), xs8, st, r);
     else
-      s = d->E <= 128 ? launch(rtc_select_kernel<16, 4>, sg, dim3(256), 0, st, r)
-                      : launch(rtc_select_kernel<16, 8>, sg, dim3(256), 0, st, r);
+      s = d->E <= 128 ? launch(rtc_select_kernel<16, 4>, sg, dim3(256), xs16, st, r)
+                      : launch(rtc_select_kernel<16, 8>, sg, dim3(256), xs16, st, r);
     if (s != FTMOE_OK) return s;
     return launch(rtc_fallback_kernel, dim3(sms), dim3(256), 0, st, r);
   }

@@ -294,13 +294,16 @@ __device__ __forceinline__ void rtc_write(const RtcArgs& a, int t, int lane, flo
 //      and weights of the CUDA-core router.
 // A token with more than 32 candidates, or a non-finite V~ or bound, goes to the fallback list.
 template <int SMAX, int EJ>
-__global__ void __launch_bounds__(256, SMAX == 8 ? 2 : 1) rtc_select_kernel(RtcArgs a) {
+__global__ void __launch_bounds__(256, SMAX == 8 ? 3 : 2) rtc_select_kernel(RtcArgs a) {
   pdl_wait();
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int S = a.d >> 8;
   constexpr int NONE = 0x7FFFFFFF;
   __shared__ float s_wmax;
   __shared__ int s_cand[8][36];
+  // the warp's token x, chunk s of lane l at [s * 32 + l] (dynamic: 8 warps x SMAX x 512 bytes)
+  extern __shared__ uint4 rtc_sx[];
+  uint4* sx = rtc_sx + wib * SMAX * 32;
   if (threadIdx.x < 32) {
     float m = 0.f;
     for (int e = lane; e < a.E; e += 32) m = fmaxf(m, a.wnorm[e]);
@@ -313,11 +316,15 @@ __global__ void __launch_bounds__(256, SMAX == 8 ? 2 : 1) rtc_select_kernel(RtcA
   const float gamma = rtc_gamma(a.d);
   unsigned n_extra = 0;
   for (int t = blockIdx.x * 8 + wib; t < a.T; t += gridDim.x * 8) {
-    // x of the token (for its norm and the order-R logits of the candidates)
+    // x of the token (for its norm here, and from shared memory for the candidates' logits)
     uint4 xv[SMAX];
     const uint4* xr = reinterpret_cast<const uint4*>(a.x + size_t(t) * a.d);
 #pragma unroll
     for (int s = 0; s < SMAX; ++s) xv[s] = s < S ? __ldg(xr + s * 32 + lane) : make_uint4(0, 0, 0, 0);
+    __syncwarp();                       // the previous token's reads of sx are done
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s)
+      if (s < S) sx[s * 32 + lane] = xv[s];
     float v[EJ];
     const float* row = a.logits + size_t(t) * a.E;
     bool fin = true;
@@ -389,7 +396,8 @@ __global__ void __launch_bounds__(256, SMAX == 8 ? 2 : 1) rtc_select_kernel(RtcA
     }
     n_extra += (n > a.k);
     __syncwarp();
-    // 3. the candidates' order-R values, four at a time (two packed pairs of chains)
+    // 3. the candidates' order-R values, four at a time (two packed pairs of chains); the
+    //    router rows' next chunks load while the current ones are used
     const int my_i = lane < n ? s_cand[wib][lane] : NONE;
     float myR = -INFINITY;
     for (int p0 = 0; p0 < n; p0 += 4) {
@@ -398,15 +406,21 @@ __global__ void __launch_bounds__(256, SMAX == 8 ? 2 : 1) rtc_select_kernel(RtcA
       for (int q = 0; q < 4; ++q)
         wrow[q] = reinterpret_cast<const uint4*>(a.wr + size_t(s_cand[wib][min(p0 + q, n - 1)]) * a.d) + lane;
       uint64_t acc[2] = {0ull, 0ull};
+      uint4 wb[2][4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) wb[0][q] = __ldg(wrow[q]);
 #pragma unroll
       for (int s = 0; s < SMAX; ++s) {
         if (s < S) {
-          uint4 wv[4];
+          if (s + 1 < S) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) wv[q] = __ldg(wrow[q] + s * 32);
+            for (int q = 0; q < 4; ++q) wb[(s + 1) & 1][q] = __ldg(wrow[q] + (s + 1) * 32);
+          }
+          const uint4(&wv)[4] = wb[s & 1];
+          const uint4 xs = sx[s * 32 + lane];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const uint32_t xx = (&xv[s].x)[u >> 1];
+            const uint32_t xx = (&xs.x)[u >> 1];
             const float xf = (u & 1) ? bf16_hi(xx) : bf16_lo(xx);
             const uint64_t x2 = f32x2_pack(xf, xf);
 #pragma unroll
