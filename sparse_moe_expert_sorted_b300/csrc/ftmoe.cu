@@ -95,12 +95,14 @@ inline int cdiv(long long a, long long b) { return int((a + b - 1) / b); }
 bool route_tc_ok(const ftmoe_layer_desc* d, int T) {
   return T >= FTMOE_PREFILL_MIN_T && d->renorm == 1 && d->E >= 16 && d->E <= 256 && d->E % 16 == 0 && d->d <= 4096;
 }
-// header | logits [T][E] | (tensor-core router) expert norms [E] | fallback tokens [T]
+// header | logits [T][E] | (tensor-core router) expert norms [E] | fallback tokens [T] |
+// logits of the second half of K [T][E]
 size_t route_ws(const ftmoe_layer_desc* d, int T, bool own_logits) {
   size_t n = kWsHeader;
   if (own_logits) {
     n += align256(size_t(T) * d->E * sizeof(float));
-    if (route_tc_ok(d, T)) n += align256(size_t(d->E) * 4) + align256(size_t(T) * 4);
+    if (route_tc_ok(d, T))
+      n += align256(size_t(d->E) * 4) + align256(size_t(T) * 4) + align256(size_t(T) * d->E * sizeof(float));
   }
   return n;
 }
@@ -291,6 +293,7 @@ ftmoe_status route_impl(const ftmoe_layer_desc* d, const uint16_t* x, const uint
     char* extra = reinterpret_cast<char*>(a.logits) + align256(size_t(T) * d->E * sizeof(float));
     r.wnorm = reinterpret_cast<float*>(extra);
     r.fb_list = reinterpret_cast<int32_t*>(extra + align256(size_t(d->E) * 4));
+    r.logits2 = reinterpret_cast<float*>(extra + align256(size_t(d->E) * 4) + align256(size_t(T) * 4));
     r.fb_count = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kWsRouteFallback);
     r.extra_count = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kWsRouteExtra);
     r.ids = ids;
@@ -301,8 +304,10 @@ ftmoe_status route_impl(const ftmoe_layer_desc* d, const uint16_t* x, const uint
     s = launch(rtc_prep_kernel, dim3(std::max(1, std::min(cdiv(d->E, 8), sms))), dim3(256), 0, st, r);
     if (s != FTMOE_OK) return s;
     const int tiles = cdiv(T, kTileM);
-    s = launch(rtc_logits_kernel, dim3(std::min(tiles, sms)), dim3(kRtcThreads), size_t(rtc_smem(d->E)), st, tmX, tmW,
-               r, d->E);
+    // fewer tiles than half the SMs: two CTAs per tile, each over half of K
+    r.ksplit = (2 * tiles <= sms && (d->d / 64) % 2 == 0) ? 2 : 1;
+    s = launch(rtc_logits_kernel, dim3(std::min(tiles * r.ksplit, sms)), dim3(kRtcThreads), size_t(rtc_smem(d->E)), st,
+               tmX, tmW, r, d->E);
     if (s != FTMOE_OK) return s;
     const dim3 sg(std::min(cdiv(T, 8), sms * 4));
     const size_t xs8 = 8 * 8 * 512, xs16 = 8 * 16 * 512;   // per-warp x rows in shared memory

@@ -9,7 +9,10 @@
 // Kernels (one stream, in order; renormalised weights, 16 <= E <= 256, E % 16 == 0):
 //   rtc_prep_kernel    per expert ||W_r[e]||_2 (an upper bound, rounded up); zeroes the counts
 //   rtc_logits_kernel  tensor-core logits L~ = x W_r^T in fp32 (bf16 x bf16 products, fp32
-//                      accumulation), M = 128 tokens per tile, N = E, K = 64 per stage
+//                      accumulation), M = 128 tokens per tile, N = E, K = 64 per stage; when
+//                      the tiles fill less than half the SMs, two CTAs per tile each take half
+//                      of K and the selection adds the two parts (one more fp32 rounding,
+//                      inside the bound below)
 //   rtc_select_kernel  one warp per token: the candidates, their order-R logits, the top-k
 //   rtc_fallback_kernel  tokens with too many candidates: every logit in order R, then the
 //                      exact selection
@@ -55,7 +58,9 @@ struct RtcArgs {
   const uint16_t* wr;     // [E][d]
   const float* bias;      // [E] or nullptr
   int T, E, d, k;
-  float* logits;          // [T][E] workspace: the tensor-core logits
+  float* logits;          // [T][E] workspace: the tensor-core logits (over K / ksplit, part 0)
+  float* logits2;         // [T][E] workspace: part 1 of a split K (ksplit == 2)
+  int ksplit;             // 1, or 2: two CTAs per 128-token tile, each over half of K
   float* wnorm;           // [E] workspace: ||W_r[e]||_2, rounded up
   int32_t* fb_list;       // [T] workspace: tokens left to the fallback
   unsigned* fb_count;     // workspace header word: their number (zeroed by rtc_prep_kernel)
@@ -133,15 +138,17 @@ rtc_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tslot;
-  const int tiles = (a.T + kTileM - 1) / kTileM;
-  const int KS = a.d / 64;
+  // work items: (tile, part of K); item i = tile * ksplit + part
+  const int tiles = (a.T + kTileM - 1) / kTileM * a.ksplit;
+  const int KS = a.d / 64 / a.ksplit;
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       uint32_t stage = 0, ph = 0;
       int issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+      for (int item = blockIdx.x; item < tiles && ok; item += gridDim.x) {
+        const int tile = item / a.ksplit, k0 = (item % a.ksplit) * KS;
         for (int ks = 0; ks < KS; ++ks) {
           if (!mbar_wait(bar_empty + 8 * stage, ph ^ 1, s_abort)) {
             ok = false;
@@ -149,8 +156,8 @@ rtc_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
           }
           const uint32_t fb = bar_full + 8 * stage;
           mbar_arrive_expect_tx(fb, uint32_t(A_BYTES + B_BYTES));
-          tma_load_2d(sb + stage * A_BYTES, &tmX, ks * 128, tile * kTileM, fb);
-          tma_load_2d(sb + OFF_B + stage * B_BYTES, &tmW, ks * 128, 0, fb);
+          tma_load_2d(sb + stage * A_BYTES, &tmX, (k0 + ks) * 128, tile * kTileM, fb);
+          tma_load_2d(sb + OFF_B + stage * B_BYTES, &tmW, (k0 + ks) * 128, 0, fb);
           ++issued;
           if (++stage == kRtcStages) {
             stage = 0;
@@ -215,7 +222,7 @@ rtc_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
     const int q = warp & 3;              // TMEM lane quarter of this warp
     const int r = q * 32 + lane;
     uint32_t tph = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    for (int item = blockIdx.x; item < tiles; item += gridDim.x) {
       if (!mbar_wait(bar_tfull, tph, s_abort)) {
         if (lane == 0) {
           set_dev_err(DEV_ERR_TIMEOUT);
@@ -224,7 +231,8 @@ rtc_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         break;
       }
       tc_fence_after();
-      const int t = tile * kTileM + r;
+      const int t = (item / a.ksplit) * kTileM + r;
+      float* out = (item % a.ksplit) ? a.logits2 : a.logits;
       const uint32_t tb = tmem + (uint32_t(q * 32) << 16);
       for (int c0 = 0; c0 < N; c0 += 16) {
         uint32_t v[16];
@@ -232,7 +240,7 @@ rtc_logits_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant
         tc_wait_ld();
         tc_reg_fence(v);
         if (t < a.T) {
-          float* dst = a.logits + size_t(t) * a.E + c0;
+          float* dst = out + size_t(t) * a.E + c0;
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             if (c0 + i < a.E) dst[i] = __uint_as_float(v[i]);
@@ -327,13 +335,14 @@ __global__ void __launch_bounds__(256, SMAX == 8 ? 3 : 2) rtc_select_kernel(RtcA
       if (s < S) sx[s * 32 + lane] = xv[s];
     float v[EJ];
     const float* row = a.logits + size_t(t) * a.E;
+    const float* row2 = a.logits2 + size_t(t) * a.E;
     bool fin = true;
 #pragma unroll
     for (int j = 0; j < EJ; ++j) {
       const int e = j * 32 + lane;
       v[j] = -INFINITY;
       if (e < a.E) {
-        const float l = __ldcg(row + e);
+        const float l = a.ksplit == 2 ? __fadd_rn(__ldcg(row + e), __ldcg(row2 + e)) : __ldcg(row + e);
         v[j] = a.bias ? __fadd_rn(l, __ldg(a.bias + e)) : l;
         fin = fin && isfinite(v[j]);
       }

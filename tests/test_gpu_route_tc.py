@@ -57,14 +57,21 @@ def _both(dsc, x, wr, bias):
     torch.cuda.synchronize()
     words = ws.view(torch.int32)
     fb, extra = int(words[FALLBACK_WORD].item()), int(words[EXTRA_WORD].item())
-    tc_logits = ws[ft.WS_ZERO_BYTES:ft.WS_ZERO_BYTES + T * dsc.E * 4].view(torch.float32).view(T, dsc.E)
+    a256 = lambda n: (n + 255) // 256 * 256
+    part = lambda o: ws[o:o + T * dsc.E * 4].view(torch.float32).view(T, dsc.E).double()
+    tc_logits = part(ft.WS_ZERO_BYTES)
+    # with fewer 128-token tiles than half the SMs the library splits K in two; the second part
+    # follows the expert norms and the fallback list
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if 2 * ((T + 127) // 128) <= sms and (dsc.d // 64) % 2 == 0:
+        tc_logits = tc_logits + part(ft.WS_ZERO_BYTES + a256(T * dsc.E * 4) + a256(dsc.E * 4) + a256(T * 4))
     # the largest logit error relative to ||x|| max ||w_e|| (bias removed in fp64)
     lr = logits.double().cpu()
     if bias is not None:
         lr = lr - bias.double().cpu()
     xn = x.double().cpu().norm(dim=1)
     wn = wr.double().cpu().norm(dim=1).max()
-    rel = float(((tc_logits.double().cpu() - lr).abs().max(dim=1).values / (xn * wn)).max())
+    rel = float(((tc_logits.cpu() - lr).abs().max(dim=1).values / (xn * wn)).max())
     return ids_tc, w_tc, ids_r, w_r, fb, extra, rel
 
 
