@@ -557,18 +557,26 @@ def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
                 oh.copy_(ob, non_blocking=True)
         how = "per step: pinned H2D of x, ftmoe_layer_forward per layer, D2H of the bf16 output; wall clock"
     else:
-        ws = ft.workspace(ft.layer_host_workspace_size(dsc, T))
+        # two streams, each with its own workspace and output buffers, take alternate steps, as a
+        # serving loop would: one step's host copies overlap the other's compute (the link is
+        # full duplex).  Every step still copies its own x in and its own output out.
+        streams = [main, torch.cuda.Stream()]
+        wss = [ft.workspace(ft.layer_host_workspace_size(dsc, T)) for _ in streams]
+        ohs = [oh, torch.empty(T, L.d, dtype=torch.bfloat16).pin_memory()]
+        dev_out = [(ids, tw, of), (torch.empty_like(ids), torch.empty_like(tw), torch.empty_like(of))]
         calls = {}
         for i in range(len(xh)):
             for li in range(n_layers):
                 l = layers[li]
-                calls[i, li] = ft.LayerHostCall(dsc, structs[li], None, xh[i], l.wr, l.bias, ids, tw, of, oh, ws,
-                                                main)
+                for j in range(2):
+                    i_, w_, o_ = dev_out[j]
+                    calls[i, li, j] = ft.LayerHostCall(dsc, structs[li], None, xh[i], l.wr, l.bias, i_, w_, o_,
+                                                       ohs[j], wss[j], streams[j])
 
         def step(i):
-            calls[i % len(xh), i % n_layers]()
+            calls[i % len(xh), i % n_layers, i % 2]()
         how = ("per step: one ftmoe_layer_forward_host call (pinned H2D of x, the layer, D2H of the bf16 output), "
-               "arguments packed once; wall clock")
+               "arguments packed once; steps alternate between two streams with their own buffers; wall clock")
 
     for i in range(5):
         step(i)
@@ -577,7 +585,7 @@ def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
     for i in range(steps):
         step(i)
     t_issue = time.perf_counter() - t0
-    main.synchronize()
+    torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     return {"value": round(T * steps / dt, 3), "unit": "tokens/s", "h2d_bytes_per_step": T * L.d * 2,
             "d2h_bytes_per_step": T * L.d * 2, "steps": steps,
