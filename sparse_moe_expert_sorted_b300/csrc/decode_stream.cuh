@@ -129,6 +129,7 @@ __global__ void prep_decode_kernel(const uint8_t* gate, const uint8_t* up, const
 
 constexpr int kSdMaxStages = 6;
 constexpr int kSdRedBufs = 2;       // reduction buffers at most (items alternate between them)
+constexpr int kSdCopyPieces = 8;    // bulk copies per streamed weight block
 constexpr int kSdRouteMaxT = 8;     // tokens the fused router takes (one token group per expert)
 
 // Layout of one stage and of the kernel's shared memory, for one (d, f, format).  A stage
@@ -810,7 +811,7 @@ sd_ffn_kernel(FfnArgs a, SdLayout Ls, SdRoute ra, unsigned long long* gsync) {
           const uint8_t* src = a.prep_dec + size_t(it.slot) * slot_bytes +
                                (phase ? size_t(a.f / kSdRowsA) * blk_a + size_t(it.n0) * blk_b
                                       : size_t(it.n0) * blk_a);
-          bulk_load(smem_u32(sm + stage * Ls.stage_bytes), src, bytes, bars + 8 * stage);
+          bulk_load_split(smem_u32(sm + stage * Ls.stage_bytes), src, bytes, bars + 8 * stage, kSdCopyPieces);
         }
         __syncwarp();
         if (++stage == uint32_t(S)) {
@@ -1546,10 +1547,11 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
         const uint32_t full = bars + 8 * stage;
         mbar_arrive_expect_tx(full, uint32_t(blk_a + size_t(sl_slice_bytes(a.d))));
         uint8_t* dst = sm + stage * Ls.stage_bytes;
-        bulk_load(smem_u32(dst), a.prep_dec + size_t(it.slot) * slot_bytes + size_t(it.n0) * blk_a, uint32_t(blk_a),
-                  full);
-        bulk_load(smem_u32(dst + Ls.off_d), slices + size_t(it.slot) * slice_slot + size_t(it.n0) * sl_slice_bytes(a.d),
-                  uint32_t(sl_slice_bytes(a.d)), full);
+        bulk_load_split(smem_u32(dst), a.prep_dec + size_t(it.slot) * slot_bytes + size_t(it.n0) * blk_a,
+                        uint32_t(blk_a), full, kSdCopyPieces);
+        bulk_load_split(smem_u32(dst + Ls.off_d),
+                        slices + size_t(it.slot) * slice_slot + size_t(it.n0) * sl_slice_bytes(a.d),
+                        uint32_t(sl_slice_bytes(a.d)), full, kSdCopyPieces);
       }
       __syncwarp();
       if (++stage == uint32_t(S)) {

@@ -129,6 +129,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+// One logical bulk copy issued as `pieces` equal copies on the same mbarrier (one piece when
+// the size does not split into multiples of 16 bytes).  Measured on B300: the one-token decode
+// layer's 54 KB items stream ~1.3% faster as eight copies than as two.
+__device__ __forceinline__ void bulk_load_split(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                                int pieces) {
+  if (pieces < 1 || bytes % (16u * uint32_t(pieces)) != 0) pieces = 1;
+  const uint32_t p = bytes / uint32_t(pieces);
+  for (int i = 0; i < pieces; ++i) bulk_load(dst + uint32_t(i) * p, static_cast<const uint8_t*>(src) + size_t(i) * p, p, bar);
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

@@ -81,8 +81,10 @@ def _check_oracle(ids, w, x, wr, bias_np, k, rows):
     np.testing.assert_allclose(w.cpu().numpy()[rows], o_w, rtol=2e-6, atol=1e-7)
 
 
+# 12288 tokens: 96 tiles, more than half the SMs, so the logits run without the split of K
 @pytest.mark.parametrize("E,k,d,T,zipf", [(128, 8, 2048, 8192, 0.0), (128, 8, 2048, 1000, 1.1), (256, 6, 4096, 300, 1.0),
-                                          (16, 4, 256, 256, 0.0), (64, 32, 1024, 520, 0.0)])
+                                          (16, 4, 256, 256, 0.0), (64, 32, 1024, 520, 0.0),
+                                          (256, 6, 4096, 12288, 1.0)])
 def test_tensor_core_router_equals_order_r_and_the_oracle(E, k, d, T, zipf):
     seed = E + T
     dsc = ft.desc(E, k, d, 256, synth.NVFP4, 1)
