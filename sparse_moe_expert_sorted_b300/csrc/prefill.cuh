@@ -646,8 +646,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
       }
       if (MODE == 1 && a.topk_w) {
-        // Fused combine.  Stage w * y of the warp's 32 rows, then add row by row so that
-        // every vector reduction of the warp covers contiguous columns of one or two rows.
+        // Fused combine.  Each lane stages w * y of its row in shared memory and hands it to
+        // one asynchronous bulk reduce-add into out[token] (the reductions run beside the next
+        // tile's epilogue; a lane's staging row is rewritten only after its reduction read it).
         constexpr int NB = NH / 32;
         constexpr int HC = NH / 2;                  // columns of this warp
         float* stg = reinterpret_cast<float*>(smem + Cfg::OFF_STG) + (warp - 2) * 32 * Cfg::STG_STRIDE;
@@ -660,6 +661,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
         for (int b = 0; b < NB; ++b) tc_reg_fence(v[b]);
         release();
+        // the staging of the previous tile has been read by its bulk reductions
+        bulk_wait_read0();
+        __syncwarp();
         float* my = stg + lane * Cfg::STG_STRIDE;
 #pragma unroll
         for (int b = 0; b < NB; ++b)
@@ -668,23 +672,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             reinterpret_cast<float4*>(my + 16 * b)[i4] =
                 make_float4(w * __uint_as_float(v[b][4 * i4]), w * __uint_as_float(v[b][4 * i4 + 1]),
                             w * __uint_as_float(v[b][4 * i4 + 2]), w * __uint_as_float(v[b][4 * i4 + 3]));
-        __syncwarp();
-        constexpr int LPR = HC / 4;                 // lanes per row (float4 each)
-        constexpr int RPI = 32 / LPR;               // rows per instruction
-        const int sub = lane / LPR, cl = lane % LPR;
-        const int col0 = nt * NH + half * HC;
-#pragma unroll 4
-        for (int r0 = 0; r0 < 32; r0 += RPI) {
-          const int rr = r0 + sub;
-          const int t_r = __shfl_sync(0xFFFFFFFFu, tok, rr);
-          const float4 val = reinterpret_cast<const float4*>(stg + rr * Cfg::STG_STRIDE)[cl];
-          if (t_r >= 0) atomicAdd(reinterpret_cast<float4*>(a.out + size_t(t_r) * a.d + col0) + cl, val);
+        // each lane's row, HC floats, is added into out[token] by one bulk reduction
+        fence_proxy_async_smem();
+        if (tok >= 0) {
+          bulk_reduce_add_f32(a.out + size_t(tok) * a.d + nt * NH + half * HC, smem_u32(my), uint32_t(HC * 4));
         }
-        __syncwarp();
+        bulk_commit();
       }
       acc ^= 1;
       if (acc == 0) aph ^= 1;
     }
+    if (MODE == 1) bulk_wait0();   // the fused combine's reductions have completed
   }
   tc_fence_before();
   __syncthreads();

@@ -138,6 +138,20 @@ __device__ __forceinline__ void bulk_load_split(uint32_t dst, const void* src, u
   const uint32_t p = bytes / uint32_t(pieces);
   for (int i = 0; i < pieces; ++i) bulk_load(dst + uint32_t(i) * p, static_cast<const uint8_t*>(src) + size_t(i) * p, p, bar);
 }
+// Bulk reduce-add of fp32 from shared to global memory (both 16-byte aligned, size a multiple
+// of 16), in the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_reduce_add_f32(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// waits until the thread's bulk groups have finished reading their shared-memory sources
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// waits until the thread's bulk groups have completed
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// orders this thread's generic-proxy shared-memory writes before later async-proxy reads
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
