@@ -119,9 +119,8 @@ typedef struct {
  *      layout holds the 512 bytes that fill four tensor-memory columns there: byte
  *      (r % 32) * 16 + (r / 32) * 4 + kb for row r of the 128 and 16-element
  *      block kb of the 64.  The tensor-core path reads the codes in place.
- *        gate/up  [C][ffn/NH][d/64][A][512]: an N tile of NH gate rows then NH up
- *                 rows (NH = 96 if ffn % 96 == 0, else 64) in A = ceil(2*NH/128)
- *                 blocks of 128 rows, zero past 2*NH rows
+ *        gate/up  [C][ffn/NH][d/64][A][512]: an N tile of NH = 128 gate rows then
+ *                 NH up rows in A = 2 blocks of 128 rows
  *        down     [C][d/128][ffn/64][512]
  *   2. Decode (NVFP4, MXFP4), starting at the next 1024-byte boundary: a copy of
  *      codes and scales in tiles that each stream into shared memory with one

@@ -129,7 +129,7 @@ bool path0_size_ok(const ftmoe_layer_desc* d, int T) {
   return groups * std::max(d->d, d->ffn) <= (1ll << 28);
 }
 // N tile of the gate/up GEMM: NH gate rows + NH up rows
-int gate_up_nh(const ftmoe_layer_desc* d) { return d->ffn % 96 == 0 ? 96 : 64; }
+int gate_up_nh(const ftmoe_layer_desc* d) { return d->ffn % 128 == 0 ? 128 : 64; }
 
 inline size_t align1k(size_t v) { return (v + 1023) & ~size_t(1023); }
 
@@ -501,8 +501,8 @@ ftmoe_status ffn_tc_impl(const ftmoe_layer_desc* d, const ftmoe_weights* w, cons
   g.topk_w = nullptr;
   g.out = nullptr;
   const int mts = int(L.rows / kTileM);
-  s = nh == 96 ? launch_gemm<0, 96>(tA1, tG, tU, g, mts * (d->ffn / 96), st)
-               : launch_gemm<0, 64>(tA1, tG, tU, g, mts * (d->ffn / 64), st);
+  s = nh == 128 ? launch_gemm<0, 128>(tA1, tG, tU, g, mts * (d->ffn / 128), st)
+                : launch_gemm<0, 64>(tA1, tG, tU, g, mts * (d->ffn / 64), st);
   if (s != FTMOE_OK) return s;
   g.sfa = sfh;
   g.sfb = prep + align1k(prep_gate_up_bytes(d, w->C));

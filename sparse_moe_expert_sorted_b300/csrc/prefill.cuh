@@ -41,12 +41,15 @@
 //   warp 0      TMA producer: A, B tiles (128-byte swizzle) and scale blocks
 //               into a kStages-deep shared-memory ring
 //   warp 1      TMEM owner and MMA issuer (one thread)
-//   warps 2-9   epilogue; warp w reads TMEM lanes 32 * (w % 4) .. + 31
-//   warps 10-13 scale writers: each stage's scale blocks, shared memory ->
+//   warps 2-17  epilogue; warp w reads TMEM lanes 32 * (w % 4) .. + 31, a
+//               quarter of each matrix's columns
+//   warps 18-21 scale writers: each stage's scale blocks, shared memory ->
 //               registers -> TMEM (tcgen05.st, one lane quarter per warp)
-// TMEM: accumulator b at column 256 b (N <= 208 columns), the scale blocks of
-// the stage in flight right after it (16 + 16 * SFB_ATOMS columns, two buffers
-// alternate).  Measured on B300: writing the scales with tcgen05.st from the
+// TMEM: the down GEMM (N = 128) double-buffers its accumulator (columns 0 and
+// 256) with the scale blocks of the stage in flight right after each (two
+// buffers alternate); the gate/up GEMM (N = 256) has one accumulator at column
+// 0, handed back as soon as the 16 epilogue warps hold it, and its two scale
+// buffers from column 256.  Measured on B300: writing the scales with tcgen05.st from the
 // scale warps costs the MMA issuer nothing, while tcgen05.cp copies issued
 // between its MMAs serialise with them (the 8192-token gate/up GEMM spent
 // ~80 us of ~210 us on them).
@@ -61,7 +64,8 @@ constexpr int kStages = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = (2 + kEpiWarps) * 32;
 constexpr int kSfWarps = 4;                                  // FP4 GEMM: scale writers
-constexpr int kGemmNvThreads = (2 + kEpiWarps + kSfWarps) * 32;
+constexpr int kNvEpiWarps = 16;                              // FP4 GEMM: epilogue warps (4 per lane quarter)
+constexpr int kGemmNvThreads = (2 + kNvEpiWarps + kSfWarps) * 32;
 constexpr int kStageK = 256;            // FP4 elements per stage (128 bytes per row)
 constexpr int kSfBlock = 512;           // bytes of one 128-row x K=64 scale block
 
@@ -356,18 +360,30 @@ struct GemmCfg {
   // full[S], empty[S], tfull[2], tempty[2], done, sf_full[2], sf_free[2], sfld[S]
   static constexpr int OFF_BAR = OFF_SFB + kStages * SFB_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + (3 * kStages + 9) * 8;
-  // TMEM columns of one stage's scales (after the accumulator): SFA 4 per K = 64 step, then
-  // SFB 4 per step and 128-row atom
+  // TMEM columns of one stage's scales: SFA 4 per K = 64 step, then SFB 4 per step and 128-row
+  // atom.  Two accumulators (columns 0 and 256) when an accumulator and a scale buffer fit in
+  // 256 columns, the scale buffers right after each; else one accumulator at column 0 and the
+  // two scale buffers from column 256.
   static constexpr int SF_COLS = 16 + 16 * SFB_ATOMS;
+  static constexpr int ACC_BUFS = N + SF_COLS <= 256 ? 2 : 1;
+  // epilogue warps at work: all 16 for gate/up; 8 for the down GEMM, whose combine then issues
+  // half as many (and twice as long) bulk reductions (measured faster)
+  static constexpr int EPI_ACTIVE = MODE == 0 ? kNvEpiWarps : 8;
+  static constexpr int EPI_COLS = NH / (EPI_ACTIVE / 4);        // columns of each matrix per epilogue warp
+  __host__ __device__ static constexpr uint32_t sf_col(uint32_t buf) {
+    return ACC_BUFS == 2 ? buf * 256 + N : 256 + buf * SF_COLS;
+  }
   static constexpr int OFF_MT = OFF_MISC + 16;                     // int s_mt[1025], s_tmp[33]
-  // MODE 1: per epilogue warp, its 32 rows x NH/2 columns of the tile (row stride padded by 4 floats)
-  static constexpr int STG_STRIDE = NH / 2 + 4;
+  // MODE 1: per epilogue warp, its 32 rows x EPI_COLS columns of the tile (row stride padded by 4 floats)
+  static constexpr int STG_STRIDE = EPI_COLS + 4;
   static constexpr int OFF_STG = (OFF_MT + (1025 + 33) * 4 + 15) / 16 * 16;
-  static constexpr int STG_BYTES = MODE == 1 ? kEpiWarps * 32 * STG_STRIDE * 4 : 0;
+  static constexpr int STG_BYTES = MODE == 1 ? EPI_ACTIVE * 32 * STG_STRIDE * 4 : 0;
   static constexpr int SMEM = OFF_STG + STG_BYTES + 1024;        // + alignment slack
   static constexpr uint32_t IDESC = idesc_mxf4(kTileM, N, 0);
   static_assert(N % 16 == 0 && N <= 256, "MMA N");
-  static_assert(N + 16 + 16 * ((N + 127) / 128) <= 256, "accumulator + scale columns must fit 256 TMEM columns");
+  static_assert(ACC_BUFS == 2 || N + 2 * SF_COLS <= 512 - 256 + N, "accumulators + scale columns within 512 TMEM columns");
+  static_assert(ACC_BUFS == 2 || 256 + 2 * SF_COLS <= 512, "scale buffers after the single accumulator");
+  static_assert(EPI_COLS % 16 == 0, "whole 16-column TMEM loads per epilogue warp");
   static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "1024-byte aligned stage buffers");
   static_assert(SMEM <= 232448, "one CTA's opt-in shared memory");
   static_assert(STAGE_TX < (1 << 20), "an mbarrier's transaction count");
@@ -400,7 +416,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_tfull + 8 * b, 1);
-      mbar_init(bar_tempty + 8 * b, kEpiWarps);
+      mbar_init(bar_tempty + 8 * b, Cfg::EPI_ACTIVE);
       mbar_init(bar_sffull + 8 * b, kSfWarps);
       mbar_init(bar_sffree + 8 * b, 1);
     }
@@ -479,7 +495,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
         if (!mbar_wait(bar_tempty + 8 * acc, aph ^ 1, s_abort)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * 256;
+        const uint32_t d_tmem = tmem + acc * 256;      // acc stays 0 with one accumulator
         for (int ks = 0; ks < KS; ++ks) {
           if (!mbar_wait(bar_full + 8 * stage, ph, s_abort) || !mbar_wait(bar_sffull + 8 * sfbuf, sfph, s_abort)) {
             ok = false;
@@ -488,7 +504,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           tc_fence_after();
           const uint32_t sA = sb + Cfg::OFF_A + stage * Cfg::A_BYTES;
           const uint32_t sB = sb + Cfg::OFF_B + stage * Cfg::B_BYTES;
-          const uint32_t sf_col = tmem + sfbuf * 256 + N;    // written by the scale warps
+          const uint32_t sf_col = tmem + Cfg::sf_col(sfbuf);   // written by the scale warps
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_nvf4(d_tmem, desc_sw128(sA + 32 * kk), desc_sw128(sB + 32 * kk), Cfg::IDESC, sf_col + 4 * kk,
@@ -501,8 +517,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
         if (!ok) break;
         tc_commit(bar_tfull + 8 * acc);
-        acc ^= 1;
-        if (acc == 0) aph ^= 1;
+        if (Cfg::ACC_BUFS == 2) {
+          acc ^= 1;
+          if (acc == 0) aph ^= 1;
+        } else {
+          aph ^= 1;
+        }
       }
       if (!ok) {
         set_dev_err(DEV_ERR_TIMEOUT);
@@ -512,13 +532,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
       tc_commit(bar_done);
       mbar_wait(bar_done, 0, nullptr);
     }
-  } else if (warp >= 2 + kEpiWarps) {
+  } else if (warp >= 2 + kNvEpiWarps) {
     // ---------------- scale writers ----------------
     // Lane l of the warp of quarter q writes TMEM lane 32 q + l: in every quarter, column
     // c of a K = 64 step holds bytes 16 l + 4 c .. + 3 of the step's 512-byte scale block
     // (the scales of row 32 c + l), the layout the block-scaled MMA reads.
     const int q = warp & 3;
-    const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16) + N;
+    const uint32_t lane_base = tmem + (uint32_t(q * 32) << 16);
     uint32_t stage = 0, ph = 0, sfbuf = 0, sfph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
@@ -537,7 +557,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           const uint4 w = sfa[kk * (kSfBlock / 16)];
           v[4 * kk] = w.x; v[4 * kk + 1] = w.y; v[4 * kk + 2] = w.z; v[4 * kk + 3] = w.w;
         }
-        const uint32_t col = lane_base + sfbuf * 256;
+        const uint32_t col = lane_base + Cfg::sf_col(sfbuf);
         tc_st16(col, v);
 #pragma unroll
         for (int h = 0; h < Cfg::SFB_ATOMS; ++h) {
@@ -564,10 +584,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
   } else {
     // ---------------- epilogue ----------------
     const int q = warp & 3;             // TMEM lane quarter of this warp
-    const int half = (warp - 2) >> 2;   // which half of the tile's columns
+    const int part = (warp - 2) >> 2;   // which part of each matrix's columns (EPI_COLS each)
     const int r = q * 32 + lane;        // row within the M-tile
     uint32_t acc = 0, aph = 0;
-    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    // warps beyond the active ones have no columns (the down GEMM)
+    for (int tile = part < Cfg::EPI_ACTIVE / 4 ? int(blockIdx.x) : tiles; tile < tiles; tile += gridDim.x) {
       const int mt = tile / NT, nt = tile % NT;
       const int e = expert_of_mtile(s_mt, a.E, mt);
       const int slot = a.slot_of ? a.slot_of[e] : e;
@@ -592,12 +613,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
       };
       if (MODE == 0) {
-        constexpr int NB = NH / 32;    // 16-column blocks per warp
+        constexpr int NB = Cfg::EPI_COLS / 16;    // 16-column blocks per warp
         uint32_t g[NB][16], u[NB][16];
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-          tc_ld16(tb + half * (NH / 2) + 16 * b, g[b]);
-          tc_ld16(tb + NH + half * (NH / 2) + 16 * b, u[b]);
+          tc_ld16(tb + part * Cfg::EPI_COLS + 16 * b, g[b]);
+          tc_ld16(tb + NH + part * Cfg::EPI_COLS + 16 * b, u[b]);
         }
         tc_wait_ld();
 #pragma unroll
@@ -619,23 +640,23 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
           }
           uint2 c;
           const uint32_t sc = quant_nvfp4_16_fast(hv, c);
-          const int col = nt * NH + half * (NH / 2) + 16 * b;
+          const int col = nt * NH + part * Cfg::EPI_COLS + 16 * b;
           *reinterpret_cast<uint2*>(a.hq + size_t(j) * (a.f / 2) + col / 2) = c;
           a.sfh[sf_offset(j, col / 16, fsteps)] = uint8_t(sc);
         }
       } else if (!a.topk_w) {
         // y in sorted order
-        constexpr int NB = NH / 32;
+        constexpr int NB = Cfg::EPI_COLS / 16;
         uint32_t v[NB][16];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) tc_ld16(tb + half * (NH / 2) + 16 * b, v[b]);
+        for (int b = 0; b < NB; ++b) tc_ld16(tb + part * Cfg::EPI_COLS + 16 * b, v[b]);
         tc_wait_ld();
 #pragma unroll
         for (int b = 0; b < NB; ++b) tc_reg_fence(v[b]);
         release();
         if (meta.x >= 0) {
           const float tsd = ts0;
-          float* dst = a.out + size_t(meta.x) * a.d + nt * NH + half * (NH / 2);
+          float* dst = a.out + size_t(meta.x) * a.d + nt * NH + part * Cfg::EPI_COLS;
 #pragma unroll
           for (int b = 0; b < NB; ++b)
 #pragma unroll
@@ -649,14 +670,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // Fused combine.  Each lane stages w * y of its row in shared memory and hands it to
         // one asynchronous bulk reduce-add into out[token] (the reductions run beside the next
         // tile's epilogue; a lane's staging row is rewritten only after its reduction read it).
-        constexpr int NB = NH / 32;
-        constexpr int HC = NH / 2;                  // columns of this warp
+        constexpr int NB = Cfg::EPI_COLS / 16;
+        constexpr int HC = Cfg::EPI_COLS;           // columns of this warp
         float* stg = reinterpret_cast<float*>(smem + Cfg::OFF_STG) + (warp - 2) * 32 * Cfg::STG_STRIDE;
         const int tok = meta.y;
         const float w = __int_as_float(meta.z) * ts0;
         uint32_t v[NB][16];
 #pragma unroll
-        for (int b = 0; b < NB; ++b) tc_ld16(tb + half * HC + 16 * b, v[b]);
+        for (int b = 0; b < NB; ++b) tc_ld16(tb + part * HC + 16 * b, v[b]);
         tc_wait_ld();
 #pragma unroll
         for (int b = 0; b < NB; ++b) tc_reg_fence(v[b]);
@@ -675,12 +696,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // each lane's row, HC floats, is added into out[token] by one bulk reduction
         fence_proxy_async_smem();
         if (tok >= 0) {
-          bulk_reduce_add_f32(a.out + size_t(tok) * a.d + nt * NH + half * HC, smem_u32(my), uint32_t(HC * 4));
+          bulk_reduce_add_f32(a.out + size_t(tok) * a.d + nt * NH + part * HC, smem_u32(my), uint32_t(HC * 4));
         }
         bulk_commit();
       }
-      acc ^= 1;
-      if (acc == 0) aph ^= 1;
+      if (Cfg::ACC_BUFS == 2) {
+        acc ^= 1;
+        if (acc == 0) aph ^= 1;
+      } else {
+        aph ^= 1;
+      }
     }
     if (MODE == 1) bulk_wait0();   // the fused combine's reductions have completed
   }

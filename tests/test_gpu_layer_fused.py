@@ -96,7 +96,9 @@ def test_fused_layer_matches_separate_calls_and_oracle(fmt, E, k, d, f, T, renor
     ids_s, w_s, of_s, ob_s = _separate(dsc, W, slot, x, wr, bias)
     assert torch.equal(ids, ids_s)
     assert torch.equal(w, w_s)
-    assert _same(path, of, of_s)
+    diff = (of - of_s).abs()
+    assert _same(path, of, of_s), (f"path {path}: rel L2 {rel_l2(of.cpu().numpy(), of_s.cpu().numpy()):.3e}, "
+                                   f"max abs {float(diff.max()):.3e} at {divmod(int(diff.argmax()), of.shape[1])}")
     if path == 1:
         assert torch.equal(ob, ob_s)
     ref = OF.layer(weights_to_numpy(W.to("cpu")), slot_np, bf16_bits(x.cpu()), bf16_bits(wr.cpu()), bias_np, k,
