@@ -395,7 +395,6 @@ __global__ void __launch_bounds__(kGemmNvThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
             const __grid_constant__ CUtensorMap tmB1, GemmArgs a) {
   using Cfg = GemmCfg<MODE, NH>;
-  constexpr int N = Cfg::N;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
