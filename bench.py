@@ -378,7 +378,7 @@ def bench_ours(args, rank, ws):
                                                                    "sd_ffn_kernel with the router fused") + ")",
                     "peak_source": src, "kernel_us": round(layer_us, 3), "alg_bytes_per_call": int(alg_bytes),
                     "mean_unique_experts": round(uniq_l, 2)}
-        e2e = bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, min(K, 200), main)
+        e2e = bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, e2e_steps(K, T), main)
         return finish(args, ws, wl, L, T, K, ms_max, value, stack, n_layers, eb, roofline, e2e, gpu_launches, clk,
                       lru)
 
@@ -435,7 +435,7 @@ def bench_ours(args, rank, ws):
                     "ffn_us": round(ffn_ms * 1e3, 3)}
 
     # --- end to end through the public API with host buffers ------------------
-    e2e = bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, min(K, 200), main)
+    e2e = bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, e2e_steps(K, T), main)
     return finish(args, ws, wl, L, T, K, ms_max, value, stack, n_layers, eb, roofline, e2e, gpu_launches, clk, lru)
 
 
@@ -532,11 +532,18 @@ def lru_replay(wl, T, stack, dev="cuda"):
             "how": "one ftmoe_slot_lru_replay launch per replay, cold start; synthetic iid Zipf trace"}
 
 
+def e2e_steps(K, T):
+    """Steps of the end-to-end leg: enough for ~50 ms of one-token steps, 200 of the long ones."""
+    return min(K, 2000 if T <= 64 else 200)
+
+
 def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
-    """Same metric through the public API with pinned host inputs and outputs: per step the
-    host-buffer layer call (ftmoe_layer_forward_host: H2D of x, the layer, D2H of the bf16
-    output), one prepared ctypes call each; the stack workloads copy x once and run the 8
-    layers on it.  Wall clock over the steps, and the host time spent issuing them."""
+    """Same metric through the public API with pinned host inputs and outputs.  Per step the
+    host-buffer layer call: H2D of x, the layer, D2H of the bf16 output.  The one-call
+    workloads replay it as a CUDA graph recorded once per buffer set (ftmoe_layer_graph_*) and
+    also time the direct call (ftmoe_layer_forward_host, one prepared ctypes call per step);
+    the stack workloads copy x once and run the 8 layers on it.  Wall clock over the steps, and
+    the host time spent issuing them."""
     dev = "cuda"
     xh = [synth.make_x(T, L.d, 555 + i).pin_memory() for i in range(8)]
     oh = torch.empty(T, L.d, dtype=torch.bfloat16).pin_memory()
@@ -544,6 +551,20 @@ def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
     ob = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
     ids = torch.empty(T, L.k, dtype=torch.int32, device=dev)
     tw = torch.empty(T, L.k, dtype=torch.float32, device=dev)
+
+    def run(step):
+        for i in range(5):
+            step(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(steps):
+            step(i)
+        t_issue = time.perf_counter() - t0
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        return round(T * steps / dt, 3), round(t_issue * 1e6 / steps, 2)
+
+    extra = {}
     if stack:
         xd = torch.empty(T, L.d, dtype=torch.bfloat16, device=dev)
         ws = ft.workspace(ft.layer_workspace_size(dsc, T))
@@ -556,6 +577,7 @@ def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
                     ft.layer_forward(dsc, structs[li], None, xd, l.wr, l.bias, ids, tw, of, ob, ws, main)
                 oh.copy_(ob, non_blocking=True)
         how = "per step: pinned H2D of x, ftmoe_layer_forward per layer, D2H of the bf16 output; wall clock"
+        value, issue = run(step)
     else:
         # two streams, each with its own workspace and output buffers, take alternate steps, as a
         # serving loop would: one step's host copies overlap the other's compute (the link is
@@ -564,32 +586,37 @@ def bench_e2e(ft, dsc, layers, structs, T, L, wl, stack, n_layers, steps, main):
         wss = [ft.workspace(ft.layer_host_workspace_size(dsc, T)) for _ in streams]
         ohs = [oh, torch.empty(T, L.d, dtype=torch.bfloat16).pin_memory()]
         dev_out = [(ids, tw, of), (torch.empty_like(ids), torch.empty_like(tw), torch.empty_like(of))]
-        calls = {}
-        for i in range(len(xh)):
-            for li in range(n_layers):
-                l = layers[li]
-                for j in range(2):
-                    i_, w_, o_ = dev_out[j]
-                    calls[i, li, j] = ft.LayerHostCall(dsc, structs[li], None, xh[i], l.wr, l.bias, i_, w_, o_,
-                                                       ohs[j], wss[j], streams[j])
-
-        def step(i):
-            calls[i % len(xh), i % n_layers, i % 2]()
-        how = ("per step: one ftmoe_layer_forward_host call (pinned H2D of x, the layer, D2H of the bf16 output), "
-               "arguments packed once; steps alternate between two streams with their own buffers; wall clock")
-
-    for i in range(5):
-        step(i)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(steps):
-        step(i)
-    t_issue = time.perf_counter() - t0
-    torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    return {"value": round(T * steps / dt, 3), "unit": "tokens/s", "h2d_bytes_per_step": T * L.d * 2,
-            "d2h_bytes_per_step": T * L.d * 2, "steps": steps,
-            "host_issue_us_per_step": round(t_issue * 1e6 / steps, 2), "how": how}
+        key = lambda i: (i % len(xh), i % n_layers, i % 2)
+        keys = sorted({key(i) for i in range(steps + 5)})
+        calls, graphs, graph_error = {}, {}, None
+        for k_ in keys:
+            i, li, j = k_
+            l = layers[li]
+            i_, w_, o_ = dev_out[j]
+            a_ = (dsc, structs[li], None, xh[i], l.wr, l.bias, i_, w_, o_, ohs[j], wss[j])
+            calls[k_] = ft.LayerHostCall(*a_, streams[j])
+            if graph_error is None:
+                try:
+                    graphs[k_] = ft.LayerHostGraph(*a_, stream=streams[j])
+                except ft.FtmoeError as e:   # reported in the line; the direct calls still measure e2e
+                    graph_error = str(e)
+        d_value, d_issue = run(lambda i: calls[key(i)]())
+        direct_how = ("per step: one ftmoe_layer_forward_host call (pinned H2D of x, the layer, D2H of the bf16 "
+                      "output), arguments packed once; steps alternate between two streams with their own "
+                      "buffers; wall clock")
+        if graph_error is None:
+            value, issue = run(lambda i: graphs[key(i)]())
+            how = ("per step: one replay of a CUDA graph that holds one ftmoe_layer_forward_host call (pinned H2D "
+                   "of x, the layer, D2H of the bf16 output), recorded once per buffer set by "
+                   "ftmoe_layer_graph_create; steps alternate between two streams with their own buffers; wall clock")
+            extra = {"direct_calls": {"value": d_value, "host_issue_us_per_step": d_issue, "how": direct_how}}
+        else:
+            value, issue, how = d_value, d_issue, direct_how
+            extra = {"graph_error": graph_error}
+        for g in graphs.values():
+            g.close()
+    return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": T * L.d * 2,
+            "d2h_bytes_per_step": T * L.d * 2, "steps": steps, "host_issue_us_per_step": issue, "how": how, **extra}
 
 
 # ---------------------------------------------------------------------------

@@ -521,6 +521,34 @@ ftmoe_status ftmoe_layer_forward_host(const ftmoe_layer_desc* desc, const ftmoe_
                                       const float* logit_bias, int T, int32_t* topk_ids, float* topk_w,
                                       float* out_f32, uint16_t* out_host, void* ws, size_t ws_bytes, void* stream);
 
+/* ftmoe_layer_graph - one ftmoe_layer_forward_host call recorded once as a CUDA graph and
+ * replayed: a decode step of one token issues a copy in, one kernel and a copy out, and a
+ * replay costs the host one graph launch instead of three stream operations and the checks
+ * around them.
+ *   ftmoe_layer_graph_create takes the arguments of ftmoe_layer_forward_host, checks them the
+ *   same way, and records the call by stream capture on `stream` (a stream created by the
+ *   caller: the legacy default stream cannot be captured; NULL is FTMOE_ERR_INVALID_ARG, as is
+ *   a stream already being captured).  Nothing runs at creation.  The pointers are bound into
+ *   the graph: every replay copies from x_host and writes out_host, topk_ids, topk_w and
+ *   out_f32 as one ftmoe_layer_forward_host call with those arguments would, so the caller
+ *   keeps every buffer alive and refills x_host (pinned) between replays; a replay reads the
+ *   weights, router and slot table at their bound addresses as they are when it runs.
+ *   The caller owns *out; on failure *out is NULL and the stream is no longer capturing.
+ *   ftmoe_layer_graph_launch replays on `stream` (any stream of the graph's device; NULL =
+ *   the legacy default stream).  Replays on one workspace must not overlap (the rule of the
+ *   layer call), so replays of one graph on two streams need an order between them.
+ *   ftmoe_layer_graph_destroy frees the graph (NULL is a no-op); replays already issued
+ *   still complete.
+ * Results equal those of ftmoe_layer_forward_host with the same arguments. */
+typedef struct ftmoe_layer_graph ftmoe_layer_graph;
+ftmoe_status ftmoe_layer_graph_create(const ftmoe_layer_desc* desc, const ftmoe_weights* weights,
+                                      const int32_t* slot_of, const uint16_t* x_host, const uint16_t* w_router,
+                                      const float* logit_bias, int T, int32_t* topk_ids, float* topk_w,
+                                      float* out_f32, uint16_t* out_host, void* ws, size_t ws_bytes, void* stream,
+                                      ftmoe_layer_graph** out);
+ftmoe_status ftmoe_layer_graph_launch(ftmoe_layer_graph* graph, void* stream);
+ftmoe_status ftmoe_layer_graph_destroy(ftmoe_layer_graph* graph);
+
 /* ---------------------------------------------------------------------------
  * Helpers
  * ------------------------------------------------------------------------- */

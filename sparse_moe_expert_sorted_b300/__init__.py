@@ -35,7 +35,8 @@ EXPORTS = [
     "ftmoe_layer_workspace_size", "ftmoe_layer_path", "ftmoe_layer_forward", "ftmoe_status_string", "ftmoe_get_device_error",
     "ftmoe_version", "ftmoe_copy_slots", "ftmoe_qstar", "ftmoe_qstar_fill_count", "ftmoe_miss_split",
     "ftmoe_lru_capacity", "ftmoe_lru_resize", "ftmoe_layer_host_workspace_size", "ftmoe_layer_forward_host",
-    "ftmoe_layers_streamed", "ftmoe_set_wait_limit",
+    "ftmoe_layers_streamed", "ftmoe_set_wait_limit", "ftmoe_layer_graph_create", "ftmoe_layer_graph_launch",
+    "ftmoe_layer_graph_destroy",
 ]
 
 
@@ -106,6 +107,10 @@ def lib() -> ctypes.CDLL:
         "ftmoe_layer_forward_host": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
         "ftmoe_layers_streamed": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _I, _P, _P, _P, _SZ, _P, _P]),
         "ftmoe_set_wait_limit": (_I, [ctypes.c_ulonglong]),
+        "ftmoe_layer_graph_create": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P,
+                                          ctypes.POINTER(_P)]),
+        "ftmoe_layer_graph_launch": (_I, [_P, _P]),
+        "ftmoe_layer_graph_destroy": (_I, [_P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -522,6 +527,38 @@ class LayerHostCall:
         st = self._fn(*self._args)
         if st:
             _check(st, "ftmoe_layer_forward_host")
+
+
+class LayerHostGraph(LayerHostCall):
+    """The same call recorded once as a CUDA graph (ftmoe_layer_graph_create) and replayed by
+    each call (ftmoe_layer_graph_launch) on `stream`, or on the stream given to the call.
+    `stream` is required: the capture needs a stream the caller created."""
+
+    def __init__(self, *args, stream=None, **kw):
+        if stream is None:
+            raise FtmoeError("LayerHostGraph: a stream is required for the capture")
+        super().__init__(*args, stream=stream, **kw)
+        h = _P()
+        _check(lib().ftmoe_layer_graph_create(*self._args, ctypes.byref(h)), "ftmoe_layer_graph_create")
+        self._h = h
+        self._launch = lib().ftmoe_layer_graph_launch
+        self._st = _stream(stream)
+
+    def __call__(self, stream=None):
+        st = self._launch(self._h, self._st if stream is None else _stream(stream))
+        if st:
+            _check(st, "ftmoe_layer_graph_launch")
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().ftmoe_layer_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def layers_streamed(dsc, pool, arenas, xs, routers, biases, outs_f32, outs_bf16, ws, stream=None, copy_stream=None):

@@ -1356,6 +1356,67 @@ extern "C" ftmoe_status ftmoe_layer_forward_host(const ftmoe_layer_desc* d, cons
 }
 
 // =============================================================================
+// ftmoe_layer_graph: one host-buffer layer call captured from `stream` and instantiated.
+// =============================================================================
+struct ftmoe_layer_graph {
+  cudaGraphExec_t exec;
+};
+
+extern "C" ftmoe_status ftmoe_layer_graph_create(const ftmoe_layer_desc* d, const ftmoe_weights* w,
+                                                 const int32_t* slot_of, const uint16_t* x_host, const uint16_t* wr,
+                                                 const float* bias, int T, int32_t* ids, float* tw, float* out_f32,
+                                                 uint16_t* out_host, void* ws, size_t ws_bytes, void* stream,
+                                                 ftmoe_layer_graph** out) {
+  if (!out) return FTMOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!stream) return FTMOE_ERR_INVALID_ARG;
+  // the host checks of the call itself, before any CUDA call
+  if (!desc_ok(d) || T < 1 || T > kMaxT || !x_host || !out_host || !ws || !wr || !out_f32) return FTMOE_ERR_INVALID_ARG;
+  if ((ids == nullptr) != (tw == nullptr) || !weights_ok(d, w)) return FTMOE_ERR_INVALID_ARG;
+  if (ws_bytes < ftmoe_layer_host_workspace_size(d, T)) return FTMOE_ERR_WORKSPACE;
+  cudaStream_t st = as_stream(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return FTMOE_ERR_CUDA;
+  if (cap != cudaStreamCaptureStatusNone) return FTMOE_ERR_INVALID_ARG;
+  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return FTMOE_ERR_CUDA;
+  const ftmoe_status s =
+      ftmoe_layer_forward_host(d, w, slot_of, x_host, wr, bias, T, ids, tw, out_f32, out_host, ws, ws_bytes, stream);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(st, &g);   // always: the stream leaves capture mode
+  if (s != FTMOE_OK || e != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    (void)cudaGetLastError();
+    return s != FTMOE_OK ? s : FTMOE_ERR_CUDA;
+  }
+  cudaGraphExec_t x = nullptr;
+  const cudaError_t ie = cudaGraphInstantiate(&x, g, 0);
+  cudaGraphDestroy(g);
+  if (ie != cudaSuccess || !x) {
+    (void)cudaGetLastError();
+    return FTMOE_ERR_CUDA;
+  }
+  ftmoe_layer_graph* h = new (std::nothrow) ftmoe_layer_graph{x};
+  if (!h) {
+    cudaGraphExecDestroy(x);
+    return FTMOE_ERR_CUDA;
+  }
+  *out = h;
+  return FTMOE_OK;
+}
+
+extern "C" ftmoe_status ftmoe_layer_graph_launch(ftmoe_layer_graph* h, void* stream) {
+  if (!h) return FTMOE_ERR_INVALID_ARG;
+  return cudaGraphLaunch(h->exec, as_stream(stream)) == cudaSuccess ? FTMOE_OK : FTMOE_ERR_CUDA;
+}
+
+extern "C" ftmoe_status ftmoe_layer_graph_destroy(ftmoe_layer_graph* h) {
+  if (!h) return FTMOE_OK;
+  const cudaError_t e = cudaGraphExecDestroy(h->exec);
+  delete h;
+  return e == cudaSuccess ? FTMOE_OK : FTMOE_ERR_CUDA;
+}
+
+// =============================================================================
 // ftmoe_layers_streamed: L layers whose experts stream from a host pool through one or two
 // device arenas; with two, layer l+1's experts are copied while layer l computes.
 // =============================================================================

@@ -384,6 +384,30 @@ def test_host_buffer_layer_call_checks(L):
     assert L.ftmoe_layer_forward_host(*bad, need, None) == 1
 
 
+def test_layer_graph_checks_its_arguments_on_the_host(L):
+    """ftmoe_layer_graph_create refuses before any CUDA call: no output handle, no stream
+    (the legacy default stream cannot be captured), the host call's own checks; launch and
+    destroy take NULL as the header says."""
+    d = ft.desc(128, 8, 2048, 768, ft.NVFP4)
+    need = L.ftmoe_layer_host_workspace_size(ctypes.byref(d), 1)
+    w = _ws(8, d=2048, f=768)
+    h = ctypes.c_void_p(123)
+    args = [ctypes.byref(d), ctypes.byref(w), None, 16, 16, None, 1, 16, 16, 16, 16, 16]
+    assert L.ftmoe_layer_graph_create(*args, need, 16, None) == 1                    # no handle output
+    assert L.ftmoe_layer_graph_create(*args, need, None, ctypes.byref(h)) == 1       # no stream
+    assert h.value is None                                                            # *out cleared
+    assert L.ftmoe_layer_graph_create(*args, need - 1, 16, ctypes.byref(h)) == 4     # workspace too small
+    for i, v in ((3, None), (10, None), (9, None), (4, None)):                        # x, out_host, out_f32, router
+        bad = list(args)
+        bad[i] = v
+        assert L.ftmoe_layer_graph_create(*bad, need, 16, ctypes.byref(h)) == 1
+    bad = list(args)
+    bad[8] = None                                                                     # topk_w without topk_ids
+    assert L.ftmoe_layer_graph_create(*bad, need, 16, ctypes.byref(h)) == 1
+    assert L.ftmoe_layer_graph_launch(None, None) == 1
+    assert L.ftmoe_layer_graph_destroy(None) == 0
+
+
 def test_streamed_layers_check_their_arguments_on_the_host(L):
     d = ft.desc(16, 4, 256, 256, ft.NVFP4)
     pool, arena = _ws(48), _ws(16)

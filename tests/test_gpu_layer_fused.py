@@ -256,3 +256,58 @@ def test_host_buffer_call_equals_the_device_call(fmt, T):
         assert torch.equal(of, of_d)
         assert torch.equal(oh, ob_d.cpu())
     assert ft.get_device_error() == 0
+
+
+@pytest.mark.parametrize("fmt,E,k,d,f,T", [(synth.NVFP4, 32, 4, 512, 256, 1),     # slice form
+                                           (synth.MXFP4, 32, 4, 512, 256, 3),     # one kernel, merge form
+                                           (synth.NVFP4, 32, 4, 512, 256, 16),    # separate steps
+                                           (synth.NVFP4, 32, 4, 512, 256, 512)])  # tensor-core router and GEMMs
+def test_graph_replay_equals_the_host_call(fmt, E, k, d, f, T):
+    """ftmoe_layer_graph_create records one host-buffer layer call; each replay reads x_host as
+    it is then.  Two replays with different tokens refilled into the same pinned buffer give
+    the direct call's outputs: bit for bit where the layer call is deterministic (one kernel,
+    T <= 8), within fp32 reassociation where a fused combine adds in arrival order (T > 8).
+    The one-token replay also matches the oracle."""
+    W = synth.make_experts(fmt, E, d, f, 91, device="cuda")
+    dsc = ft.desc(E, k, d, f, fmt)
+    ft.prepare_weights(dsc, W)
+    wr = synth.make_router(E, d, 91, device="cuda")
+    st = ft.weights_struct(W)
+    stream = torch.cuda.Stream()
+    bufs = []
+    for _ in range(2):   # [0]: the graph's buffers, [1]: the direct call's
+        bufs.append(dict(ws=ft.workspace(ft.layer_host_workspace_size(dsc, T)),
+                         ids=torch.empty(T, k, dtype=torch.int32, device="cuda"),
+                         w=torch.empty(T, k, dtype=torch.float32, device="cuda"),
+                         of=torch.empty(T, d, dtype=torch.float32, device="cuda"),
+                         xh=torch.empty(T, d, dtype=torch.bfloat16).pin_memory(),
+                         oh=torch.full((T, d), float("nan"), dtype=torch.bfloat16).pin_memory()))
+    g, h = bufs
+
+    def args(b):
+        return (dsc, st, None, b["xh"], wr, None, b["ids"], b["w"], b["of"], b["oh"], b["ws"])
+
+    direct = ft.LayerHostCall(*args(h), stream)
+    graph = ft.LayerHostGraph(*args(g), stream=stream)
+    try:
+        for seed in (12, 13):
+            x = synth.make_x(T, d, seed)
+            g["xh"].copy_(x)
+            h["xh"].copy_(x)
+            graph()
+            direct()
+            stream.synchronize()
+            assert torch.equal(g["ids"], h["ids"]) and torch.equal(g["w"], h["w"])
+            if T > 8:   # the fused combine adds in arrival order
+                assert rel_l2(g["of"].cpu().numpy(), h["of"].cpu().numpy()) <= 1e-6
+                assert rel_l2(g["oh"].float().numpy(), h["oh"].float().numpy()) <= 1e-4
+            else:
+                assert torch.equal(g["of"], h["of"]) and torch.equal(g["oh"], h["oh"])
+            if T == 1:
+                ref = OF.layer(weights_to_numpy(W.to("cpu")), np.arange(E, dtype=np.int32), bf16_bits(x),
+                               bf16_bits(wr.cpu()), None, k, 1)
+                assert np.array_equal(g["ids"].cpu().numpy(), ref["ids"])
+                assert rel_l2(g["oh"].float().numpy(), ref["out"]) < TOL
+    finally:
+        graph.close()
+    assert ft.get_device_error() == 0
