@@ -1646,7 +1646,7 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
       if (lane == 0) mbar_arrive(h_full + 8 * buf);
     }
     if (!eok && ok) set_dev_err(DEV_ERR_TIMEOUT);
-    sd_work_sync();   // (the consumers write their partial outputs and meet the grid between these)
+    sd_work_sync();   // (between these the consumers write their partials: cluster form; or meet the grid)
     sd_work_sync();
     goto tail;
   }
@@ -1799,8 +1799,11 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
   }
   if (count > 0) down_part(count - 1, pend_stage, pend_e, pend_w0, pend_w1);
   // this CTA's partial output [token][row]: this lane holds tokens 2t, 2t + 1 of rows g, g + 8.
-  // Grid form: to the workspace; cluster form: to this CTA's shared memory (the ring's bytes:
-  // every staged tile has landed and been read by now).
+  // Grid form: to the workspace; cluster form: to this CTA's shared memory, over the ring's
+  // bytes.  Every staged tile has landed by now, but another consumer warp may still be reading
+  // the down slices of the last two items (a partial of more than off_d bytes reaches stage 0's
+  // slice), so in the cluster form the consumers (and the epilogue warp) meet first.
+  if (CL) sd_work_sync();
   float* pb = CL ? reinterpret_cast<float*>(sm) : ra.part + size_t(b) * a.T * a.d;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -1818,8 +1821,7 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
   }
   if (!ok) set_dev_err(DEV_ERR_TIMEOUT);
   if (CL) {
-    sd_work_sync();   // (the epilogue warp's last two meetings)
-    sd_work_sync();
+    sd_work_sync();   // (the epilogue warp's second meeting; its first is before the writes above)
   } else {
     sd_work_sync();
     if (ct == 0) {

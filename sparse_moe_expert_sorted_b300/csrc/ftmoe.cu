@@ -1122,7 +1122,9 @@ SlClusterPlan sl_cluster_plan(const FfnArgs& a, const SlLayout& Ls) {
       cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
     for (int cs : {16, 8, 4, 2}) {
       const long long epc = (a.E + cs - 1) / cs;
+      // the ring holds this CTA's router rows, and at the end its partial output [T][d] (fp32)
       if (epc * a.d * 2 > (long long)Ls.stages * Ls.stage_bytes || num_sms() < cs) continue;
+      if ((long long)a.T * a.d * 4 > (long long)Ls.stages * Ls.stage_bytes) continue;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(num_sms() / cs * cs);
       cfg.blockDim = dim3(kSdThreads);

@@ -311,3 +311,39 @@ def test_graph_replay_equals_the_host_call(fmt, E, k, d, f, T):
     finally:
         graph.close()
     assert ft.get_device_error() == 0
+
+
+@pytest.mark.parametrize("E,k,d,f,T", [(24, 4, 256, 384, 8), (128, 8, 2048, 768, 8), (128, 8, 2048, 768, 5)])
+def test_slice_form_is_deterministic_over_many_calls(E, k, d, f, T):
+    """The slice form sums every output in a fixed order, so back-to-back calls on the same
+    inputs agree bit for bit.  These shapes put the cluster form's partial output [T][d] (fp32,
+    written over the ring at the end) across stage 0's down slice, which other consumer warps
+    read until their last item is done: a write before every warp is done would show up here as
+    a call that differs from the first."""
+    fmt = synth.NVFP4
+    seed = 7 * T + d
+    W = synth.make_experts(fmt, E, d, f, seed, device="cuda")
+    x = synth.make_x(T, d, seed, device="cuda")
+    wr = synth.make_router(E, d, seed, device="cuda")
+    dsc = ft.desc(E, k, d, f, fmt)
+    ft.prepare_weights(dsc, W)
+    slot = torch.arange(E, dtype=torch.int32, device="cuda")
+    assert ft.layer_path(dsc, ft.weights_struct(W), T) == 2
+    ws = ft.workspace(ft.layer_workspace_size(dsc, T))
+    reps = 200
+    outs = torch.full((reps, T, d), float("nan"), dtype=torch.float32, device="cuda")
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    st = ft.weights_struct(W)
+    for r in range(reps):   # back to back on one stream, no host synchronisation between calls
+        ft.layer_forward(dsc, st, slot, x, wr, None, ids, w, outs[r], None, ws)
+    torch.cuda.synchronize()
+    same = np.array([torch.equal(outs[r], outs[0]) for r in range(reps)])
+    assert same.all(), f"{int((~same).sum())} of {reps} calls differ from the first (first at {int(np.argmin(same))})"
+    _, _, of_s, _ = _separate(dsc, W, slot, x, wr, None)
+    assert _same(2, outs[0], of_s)
+    ref = OF.layer(weights_to_numpy(W.to("cpu")), np.arange(E, dtype=np.int32), bf16_bits(x.cpu()),
+                   bf16_bits(wr.cpu()), None, k, 1)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert rel_l2(outs[0].cpu().numpy(), ref["out"]) < TOL
+    assert ft.get_device_error() == 0
