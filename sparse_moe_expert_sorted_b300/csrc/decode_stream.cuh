@@ -542,10 +542,14 @@ __device__ __forceinline__ void sd_route_logits(const FfnArgs& a, const SdRoute&
 // order R (as sd_route_logits), each written into s_logit of every CTA of the cluster.  Warp cw
 // takes experts cw and cw + 16 together: x of the token is loaded once into registers with the
 // two biases, and the two experts' chains run side by side (their arithmetic is unchanged).
-// d <= 2048 (at most 8 chunks per lane).  Consumer warps.
-__device__ __forceinline__ void sl_route_logits_cl(const FfnArgs& a, const SdRoute& r, const uint8_t* srow, int ne,
-                                                   int cw, int lane, int e_first, uint32_t cl_logit, int cl_n) {
+// d <= 2048 (at most 8 chunks per lane).  Consumer warps.  The router rows arrive by one bulk
+// copy on rows_bar: a warp waits for it after issuing its first x and bias loads, so that their
+// latency overlaps the copy.  Returns false if that wait gave up (abort or wait limit).
+__device__ __forceinline__ bool sl_route_logits_cl(const FfnArgs& a, const SdRoute& r, const uint8_t* srow, int ne,
+                                                   int cw, int lane, int e_first, uint32_t cl_logit, int cl_n,
+                                                   uint32_t rows_bar, volatile int* abort) {
   const int S = a.d >> 8;    // chunks per lane (<= 8)
+  bool rows_ready = false;
   for (int i0 = cw; i0 < ne; i0 += 2 * kSdCons) {
     const int i1 = i0 + kSdCons;
     const bool two = i1 < ne;
@@ -558,6 +562,10 @@ __device__ __forceinline__ void sl_route_logits_cl(const FfnArgs& a, const SdRou
 #pragma unroll
       for (int q = 0; q < 8; ++q) xv[q] = q < S ? __ldg(xr + q * 32 + lane) : make_uint4(0, 0, 0, 0);
       const float b0 = r.bias ? __ldg(r.bias + e0) : 0.f, b1 = r.bias ? __ldg(r.bias + e1) : 0.f;
+      if (!rows_ready) {
+        if (!mbar_wait_warp(rows_bar, 0, abort)) return false;
+        rows_ready = true;
+      }
       float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -587,6 +595,7 @@ __device__ __forceinline__ void sl_route_logits_cl(const FfnArgs& a, const SdRou
       }
     }
   }
+  return true;
 }
 
 // Top-k of every token by (logit desc, id asc; NaN last), softmax weights, and the stable
@@ -1470,18 +1479,28 @@ sl_layer_kernel(FfnArgs a, SlLayout Ls, SdRoute ra, unsigned long long* gsync, c
   // every CTA of the cluster has started before any writes into another's shared memory
   if (CL) asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
   pdl_wait();
+  // slot_of (which the previous kernel may have written) is loaded here and stored into shared
+  // memory after the logits, so that its latency overlaps theirs (E <= 1024 <= 2 x 576 threads)
+  static_assert(2 * kSdThreads >= 1024, "two slot_of entries per thread");
+  int slot_v[2] = {0, 0};
   if (a.slot_of)
-    for (int e = tid; e < a.E; e += kSdThreads) s_slot[e] = a.slot_of[e];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (tid + j * kSdThreads < a.E) slot_v[j] = a.slot_of[tid + j * kSdThreads];
   if (warp >= 1 && warp <= kSdCons && ne > 0) {
-    if (mbar_wait_warp(bars + 128, 0, s_abort)) {
-      if (CL)
-        sl_route_logits_cl(a, ra, sm, ne, warp - 1, lane, e_first, smem_u32(s_logit), csz);
-      else
-        sd_route_logits(a, ra, sm, ne, warp - 1, lane, e_first, e_step);
+    bool rok;
+    if (CL) {
+      rok = sl_route_logits_cl(a, ra, sm, ne, warp - 1, lane, e_first, smem_u32(s_logit), csz, bars + 128, s_abort);
     } else {
-      *s_abort = 1;
+      rok = mbar_wait_warp(bars + 128, 0, s_abort);
+      if (rok) sd_route_logits(a, ra, sm, ne, warp - 1, lane, e_first, e_step);
     }
+    if (!rok) *s_abort = 1;
   }
+  if (a.slot_of)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (tid + j * kSdThreads < a.E) s_slot[tid + j * kSdThreads] = slot_v[j];
   __syncthreads();
   if (CL) {
     cluster_sync_all();   // every logit of the layer is now in this CTA's s_logit
