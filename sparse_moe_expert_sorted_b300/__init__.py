@@ -507,6 +507,11 @@ class LayerHostCall:
             if not isinstance(t, torch.Tensor) or t.is_cuda or t.dim() != 2 or t.shape[1] != dsc.d:
                 raise FtmoeError(f"{name}: expected a host [T, {dsc.d}] tensor")
             _need(t, name, torch.bfloat16)
+            # the library copies T * d elements from (to) the address in row order, asynchronously
+            if not t.is_contiguous():
+                raise FtmoeError(f"{name}: expected a contiguous tensor")
+            if not t.is_pinned():
+                raise FtmoeError(f"{name}: expected pinned host memory (tensor.pin_memory())")
         T = x_host.shape[0]
         if out_host.shape[0] < T:
             raise FtmoeError("out_host: fewer rows than x_host")

@@ -152,3 +152,18 @@ def test_weights_struct_checks_the_arena(fmt):
         short = synth.make_experts(fmt, 3, 256, 256, 0)
         short.glob = short.glob[:2].contiguous()
         _fails(lambda: ft.weights_struct(short), "glob")
+
+
+def test_host_buffer_call_wants_pinned_contiguous_host_tensors():
+    """LayerHostCall (and the graph form built on it) copies x in and the bf16 output out by
+    address, asynchronously: a pageable host tensor or a strided view of one is refused."""
+    ds, ws = _dsc(), t(4096, dtype=torch.uint8)
+    rest = dict(w_router=bf(E, d), bias=None, ids=i32(T, k), topk_w=t(T, k), out_f32=t(T, d))
+
+    def call(xh, oh):
+        return ft.LayerHostCall(ds, None, None, xh, rest["w_router"], None, rest["ids"], rest["topk_w"],
+                                rest["out_f32"], oh, ws)
+    _fails(lambda: call(bf(T, d), bf(T, d)), "pinned host memory")
+    _fails(lambda: call(bf(d, T).t(), bf(T, d)), "contiguous")
+    _fails(lambda: call(bf(T, d + 1), bf(T, d)), "host [T, 256]")
+    _fails(lambda: call(t(T, d), bf(T, d)), "bfloat16")
