@@ -1,7 +1,8 @@
 // Host-side check of the decode kernels' shared-memory layouts (sd_layout, sl_layout) over a
 // sweep of layer shapes: for every shape a kernel accepts, the regions are ordered, aligned,
 // large enough for what the kernels put there, and fit in the opt-in shared memory of one
-// CTA.  Prints one line per failure and "checked N layouts"; exits 1 on any failure.
+// CTA (the slice form's ring also holds the cluster form's partial output).  Prints one line
+// per failure and "checked N layouts"; exits 1 on any failure.
 #include <cstdio>
 #include "../../sparse_moe_expert_sorted_b300/csrc/decode_stream.cuh"
 
@@ -80,6 +81,9 @@ int main() {
                 CHECK(f % kSdRowsA == 0, "slice f");
                 const long long rows = (E + grid - 1) / grid;
                 CHECK(rows * d * 2 <= (long long)S.stages * S.stage_bytes, "slice router rows");
+                // the cluster form leaves each CTA's partial output [T][d] (fp32) over the ring
+                CHECK((long long)T * d * 4 <= (long long)S.stages * S.stage_bytes, "slice partial E %d d %d T %d", E,
+                      d, T);
               }
             }
           }
