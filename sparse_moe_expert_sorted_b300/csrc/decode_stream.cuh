@@ -1895,10 +1895,13 @@ tail:
       cpart[o] = v;
     }
     __syncthreads();
+    // This CTA has read the cluster's shared memory for the last time: it counts in on the cluster
+    // barrier now and waits on it just before it exits (no CTA leaves while another still reads
+    // its shared memory), so neither the count-in below nor the final sum waits for the cluster.
+    cluster_arrive_release();
     if (tid == 0)   // (release: the barrier above orders the CTA's cluster-partial writes before it)
       *s_last = atom_add_acq_rel(ccnt + crank, 1u) == unsigned(ncl - 1);
     __syncthreads();
-    cluster_sync_all();   // no CTA leaves while another still reads its shared memory
     if (*s_last) {
       // slice [lo, hi) of out: the clusters' partials in cluster order
       for (int o = lo + tid; o < hi; o += kSdThreads) {
@@ -1916,6 +1919,7 @@ tail:
       }
       if (tid == 0) ccnt[crank] = 0u;   // zero again for the next call on this workspace
     }
+    cluster_wait_acquire();
   }
 }
 
