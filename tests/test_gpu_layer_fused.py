@@ -9,7 +9,8 @@ tolerance (5e-3 relative L2):
   * T = 1 .. 8, NVFP4 and MXFP4, bias and renorm;
   * skipped experts (slot -1), including a token none of whose experts is
     resident (its output row is zero);
-  * repeated calls on one workspace (the kernel's counters start at zero each call);
+  * repeated calls on one workspace (the kernel's counters start at zero each call), and 200
+    back-to-back slice-form calls that must agree bit for bit (its sums have a fixed order);
   * the full decode layer shape (128 experts, top-8, d 2048, ffn 768).
 """
 import numpy as np
